@@ -1,0 +1,517 @@
+"""Benchmark: sharded absorbed-MLA decode + LSE merge on GB300 (one JSON line).
+
+A step is one pass of the whole hot path over one batch of the workload:
+slot map + owner-filtered append of this step's new tokens, the per-shard
+partials of every shard, and the LSE merge.  The default workload is the
+K3-shaped configuration (B=64, H=96, S=131072, N=8 token round-robin shards,
+page 64, base-2 LSE, one appended token per request per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3|dsv3|ragged|long|tiny]
+                  [--impl ours|reference] [--batch B] [--no-cpu-baseline] [--no-e2e]
+
+`value` is KV-read GB/s (sum over requests of S_b * 1152 bytes per step,
+divided by the device time per step; summed over ranks for N > 1, where every
+rank runs its own replica of the workload).  --impl reference times the fp64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "sharded MLA decode+merge: µs/step, KV-read GB/s, % of binding roofline"
+KV_ROW_BYTES = 576 * 2
+FLOP_PER_TOKEN_ROW = 2 * (576 + 512)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device_sync=True):
+    if device_sync and torch.cuda.is_available():
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_accounting(cfg, S_b):
+    """Algorithmic bytes and FLOPs of one step (what the method must move / compute)."""
+    S = [int(s) for s in S_b]
+    R = cfg.q_len * cfg.H
+    kv_bytes = sum(S) * KV_ROW_BYTES
+    q_bytes = cfg.B * R * 576 * 2
+    parts = cfg.N * cfg.B * R
+    part_bytes = parts * (512 * 2 + 4) * 2          # bf16 o_r + fp32 lse, written once and read once
+    out_bytes = cfg.B * R * (512 * (4 if cfg.out_dtype == "f32" else 2) + 4)
+    new_tokens = cfg.B * max(cfg.append, cfg.chunk)
+    append_bytes = new_tokens * KV_ROW_BYTES * 2
+    # FLOPs: every visible (token, row) pair, causal rows see S_b - q_len + t + 1 tokens
+    flops = 0
+    for s in S:
+        for t in range(cfg.q_len):
+            flops += (s - cfg.q_len + t + 1) * cfg.H * FLOP_PER_TOKEN_ROW
+    return {"kv_bytes": kv_bytes, "bytes_alg": kv_bytes + q_bytes + part_bytes + out_bytes + append_bytes,
+            "flops_alg": flops, "partial_bytes_alg": kv_bytes + q_bytes + cfg.N * cfg.B * R * (512 * 4 + 4)}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_state(cfg, device):
+    import context_sharded_mla_gb300 as dcp
+    from context_sharded_mla_gb300.step import ShardedMlaDecoder
+    dcp.load_library()
+    S = workloads.lengths(cfg)
+    bt, pool_pages = workloads.block_table(cfg, S)
+    lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
+    new = max(cfg.append, cfg.chunk)
+    out_dtype = torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16
+    dec = ShardedMlaDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE,
+                            dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E, out_dtype,
+                            torch.float32, max_append=max(cfg.B * new, 1), device=device)
+    btd = bt.to(device)
+    # cache: every request holds S_b - new tokens before the step; the step appends the rest
+    new_rows, new_pos, new_req = [], [], []
+    for b in range(cfg.B):
+        S_b = int(S[b])
+        kv_b = workloads.gen_kv(cfg, b, S_b, device)
+        pre = S_b - new
+        dec.append(kv_b[:pre].contiguous(), torch.arange(pre, device=device),
+                   torch.full((pre,), b, dtype=torch.int32, device=device), btd)
+        if new:
+            new_rows.append(kv_b[pre:].clone())
+            new_pos.append(torch.arange(pre, S_b, device=device))
+            new_req.append(torch.full((new,), b, dtype=torch.int32, device=device))
+        del kv_b
+    torch.cuda.synchronize()
+    st = {"dec": dec, "bt": btd, "S": S, "seq_lens": S.to(device), "q": workloads.gen_q(cfg, device),
+          "pool_pages": pool_pages}
+    if new:
+        st["kv_new"] = torch.cat(new_rows).contiguous()
+        st["pos"] = torch.cat(new_pos).contiguous()
+        st["req"] = torch.cat(new_req).contiguous()
+    else:
+        st["kv_new"] = st["pos"] = st["req"] = None
+    return st
+
+
+def run_ours(args, cfg, rank, world, dist, device):
+    import context_sharded_mla_gb300 as dcp
+    st = build_state(cfg, device)
+    dec = st["dec"]
+    acct = workload_accounting(cfg, st["S"])
+    stream = torch.cuda.current_stream()
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    ev_part = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+
+    def step(i=None):
+        if st["kv_new"] is not None:
+            dec.append(st["kv_new"], st["pos"], st["req"], st["bt"])
+        if i is not None:
+            ev_part[i][0].record(stream)
+        dec.partial(st["q"], st["bt"], st["seq_lens"])
+        if i is not None:
+            ev_part[i][1].record(stream)
+        dec.merge()
+
+    for _ in range(args.warmup):
+        step()
+    barrier(dist)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)                       # let the sampler take its first reading
+    barrier(dist)
+    launches0 = dcp.dcp_launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev_step[i][0].record(stream)
+        step(i)
+        ev_step[i][1].record(stream)
+    t1.record(stream)
+    barrier(dist)
+    launches = dcp.dcp_launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    part_ms = [a.elapsed_time(b) for a, b in ev_part]
+    if dec.status_bits() != 0:
+        raise RuntimeError(f"device status {dec.status_bits()} after the timed steps")
+    ms_per_step = max_over_ranks(dist, total_ms / args.steps)
+    part_ms_avg = sum(part_ms) / len(part_ms)
+
+    # end-to-end through the public API with host buffers (H2D inputs, D2H result each step)
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, cfg, st, dist, acct)
+
+    peaks = load_peaks()
+    kv_gbs = acct["kv_bytes"] / (ms_per_step * 1e-3) / 1e9
+    t_hbm = acct["bytes_alg"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = acct["flops_alg"] / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    partial_achieved = acct["partial_bytes_alg"] / (part_ms_avg * 1e-3) / 1e9
+    part_flops = acct["flops_alg"] / (part_ms_avg * 1e-3) / 1e12
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(partial_achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(partial_achieved / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(part_flops, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(part_flops / peaks["bf16_tflops"], 4)}
+    roof["traffic"] = recorded_traffic(cfg)
+    roof["kernel"] = "dcp_mla_decode_partial (all its launches, CUDA events on the launching stream)"
+    roof["peak_source"] = f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured" else "fallback"
+    result = {
+        "metric": METRIC,
+        "value": round(kv_gbs * world, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "roofline_frac_step": round(max(t_hbm, t_tc) / (ms_per_step * 1e-3), 4),
+        "step_binding_roofline": bound,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 latent rows and queries, shuffled block table)",
+        "config": config_dict(cfg, st, world),
+        "roofline": roof,
+        "partial_ms": round(part_ms_avg, 5),
+        "step_ms_median": round(statistics.median(step_ms), 5),
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    return result
+
+
+def run_e2e(args, cfg, st, dist, acct):
+    dec = st["dec"]
+    stream = torch.cuda.current_stream()
+    q_host = st["q"].cpu().pin_memory()
+    seq_host = st["S"].clone().pin_memory()
+    has_new = st["kv_new"] is not None
+    if has_new:
+        kv_host = st["kv_new"].cpu().pin_memory()
+        pos_host = st["pos"].cpu().pin_memory()
+        req_host = st["req"].cpu().pin_memory()
+    o_host = torch.empty(dec.o.shape, dtype=dec.o.dtype).pin_memory()
+    lse_host = torch.empty(dec.lse.shape, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(st["q"])
+    seq_dev = torch.empty_like(st["seq_lens"])
+    if has_new:
+        kv_dev = torch.empty_like(st["kv_new"])
+        pos_dev = torch.empty_like(st["pos"])
+        req_dev = torch.empty_like(st["req"])
+    h2d = q_host.numel() * 2 + seq_host.numel() * 8
+    if has_new:
+        h2d += kv_host.numel() * 2 + pos_host.numel() * 8 + req_host.numel() * 4
+    d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * 4
+
+    def step():
+        q_dev.copy_(q_host, non_blocking=True)
+        seq_dev.copy_(seq_host, non_blocking=True)
+        if has_new:
+            kv_dev.copy_(kv_host, non_blocking=True)
+            pos_dev.copy_(pos_host, non_blocking=True)
+            req_dev.copy_(req_host, non_blocking=True)
+            o, lse = dec.step(q_dev, st["bt"], seq_dev, kv_dev, pos_dev, req_dev)
+        else:
+            o, lse = dec.step(q_dev, st["bt"], seq_dev)
+        o_host.copy_(o, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier(dist)
+    n = max(1, min(args.steps, 200))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    barrier(dist)
+    ms = max_over_ranks(dist, t0.elapsed_time(t1) / n)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(acct["kv_bytes"] / (ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "path": "ShardedMlaDecoder.step over the C ABI, pinned host buffers"}
+
+
+def recorded_traffic(cfg):
+    """DRAM bytes per launch of the partial from a committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        import hashlib
+        src = os.path.join(ROOT, "context_sharded_mla_gb300", "csrc", "dcp_decode.cu")
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        entry = rec.get(cfg.name)
+        if not entry or entry.get("source_sha") != h:
+            return None
+        scale = entry.get("scale_to_full", 1.0)
+        return int(entry["dram_bytes_per_launch"] * scale)
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def config_dict(cfg, st, world):
+    S = st["S"]
+    d = {"workload": workloads.DESCRIPTIONS[cfg.name] if cfg.name in workloads.DESCRIPTIONS else cfg.name,
+         "B": cfg.B, "H": cfg.H, "q_len": cfg.q_len, "S_total": int(S.sum()), "S_max": int(S.max()),
+         "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P, "lse_base": "2" if cfg.base == 2 else "e",
+         "new_tokens_per_request": max(cfg.append, cfg.chunk), "out_dtype": cfg.out_dtype,
+         "partials": "fp32", "global_batch": cfg.B, "seq_len": int(S.max()),
+         "parallelism": "1 GPU holds all N shards" if world == 1 else f"{world} independent replicas",
+         "l2": f"inputs larger than L2 ({int(S.sum()) * KV_ROW_BYTES / 1e9:.2f} GB of KV per step), no flush"}
+    return d
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info()]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def time_oracle(cfg, budget_s, min_units=1, device=None):
+    """Time the fp64 oracle on whole-request units (all heads, all shards + merge) of cfg.
+
+    Inputs are the same seeded rows (drawn on `device`, copied to the host
+    before the clock starts).  Returns (kv_bytes_processed, seconds, sample description).
+    """
+    import numpy as np
+    from oracle import attention
+    S = workloads.lengths(cfg)
+    gen_dev = device or "cpu"
+    q = workloads.gen_q(cfg, gen_dev).cpu()
+    order = sorted(range(cfg.B), key=lambda b: int(S[b]))
+    done_bytes, elapsed, used = 0, 0.0, []
+    heads_all = cfg.H
+    for b in order:
+        kv = workloads.gen_kv(cfg, b, int(S[b]), gen_dev).cpu().to(torch.float64).numpy()
+        qb = q[b].to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        attention.sharded_attention(qb, kv, int(S[b]), cfg.N, cfg.I, workloads.SCALE, cfg.base)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_bytes += int(S[b]) * KV_ROW_BYTES
+        used.append(b)
+        del kv
+        if len(used) >= min_units and elapsed >= budget_s:
+            break
+    desc = (f"{len(used)} whole request(s) of {cfg.B} ({sum(int(S[b]) for b in used)} tokens, all {heads_all} "
+            f"heads, all {cfg.N} shards + merge), fp64 numpy")
+    return done_bytes, elapsed, desc
+
+
+def time_oracle_fraction(cfg, seconds_target, device=None):
+    """One bounded oracle step: request 0 restricted to enough heads to take ~seconds_target."""
+    import numpy as np
+    from oracle import attention
+    S = workloads.lengths(cfg)
+    gen_dev = device or "cpu"
+    b = int(torch.argmin(S))
+    q = workloads.gen_q(cfg, gen_dev)[b].cpu().to(torch.float64).numpy()
+    kv = workloads.gen_kv(cfg, b, int(S[b]), gen_dev).cpu().to(torch.float64).numpy()
+    # calibrate on one head
+    t0 = time.perf_counter()
+    attention.sharded_attention(q[:, :1], kv, int(S[b]), cfg.N, cfg.I, workloads.SCALE, cfg.base)
+    t1 = time.perf_counter() - t0
+    heads = int(max(1, min(cfg.H, seconds_target / max(t1, 1e-6))))
+    return b, q, kv, heads, int(S[b])
+
+
+def run_reference(args, cfg, rank, world):
+    """Times the oracle (the reference arm for this build) on a bounded sample per step."""
+    from oracle import attention
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    budget_per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    b, q, kv, heads, S_b = time_oracle_fraction(cfg, budget_per_step, dev)
+    for _ in range(args.warmup):
+        attention.sharded_attention(q[:, :heads], kv, S_b, cfg.N, cfg.I, workloads.SCALE, cfg.base)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        attention.sharded_attention(q[:, :heads], kv, S_b, cfg.N, cfg.I, workloads.SCALE, cfg.base)
+    dt = (time.perf_counter() - t0) / args.steps
+    eq_bytes = S_b * KV_ROW_BYTES * heads / cfg.H      # the share of the request's work done per step
+    value = eq_bytes / dt / 1e9
+    cores = oracle_threads()
+    sample = (f"per step: request {b} ({S_b} tokens), {heads} of {cfg.H} heads, all {cfg.N} shards + merge "
+              f"(fp64 numpy oracle); throughput counts {heads}/{cfg.H} of that request's KV bytes")
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": workloads.DESCRIPTIONS.get(cfg.name, cfg.name),
+                                                  "B": cfg.B, "H": cfg.H, "n_shards": cfg.N},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="k3", choices=sorted(workloads.DESCRIPTIONS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller case for profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_info()
+    cfg = workloads.config(args.workload)
+    if args.batch:
+        cfg = workloads.config(args.workload, B=args.batch)
+    if args.impl == "reference":
+        out = run_reference(args, cfg, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl ours needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    result = run_ours(args, cfg, rank, world, dist, device)
+    if rank == 0 and not args.no_cpu_baseline:
+        kv_bytes, secs, desc = time_oracle(cfg, args.cpu_budget, device=device)
+        result["cpu_baseline"] = {"value": round(kv_bytes / secs / 1e9, 6), "unit": "GB/s",
+                                  "cores": oracle_threads(), "kind": "oracle", "sample": desc,
+                                  "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,218 @@
+"""Python binding of libdcp_gb300 (sharded absorbed-MLA decode for GB300 / sm_103a).
+
+Argument marshalling only: every function takes torch tensors that already live
+on the GPU, checks their dtype/shape/contiguity, and forwards raw device
+pointers plus the current CUDA stream to the C ABI declared in
+``include/dcp.h``.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU path.  If the library has not been built, importing
+works but the first call raises ``RuntimeError``.
+
+Functions (same names as the C ABI):
+  dcp_count, dcp_slot_map, dcp_kv_append, dcp_mla_decode_partial,
+  dcp_mla_decode_workspace_size, dcp_lse_merge
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "DcpError", "Layout", "load_library", "library_path",
+    "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
+    "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count",
+    "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
+]
+
+DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA, DCP_ERR_WORKSPACE = 0, -1, -2, -3, -4
+DCP_LSE_BASE_E, DCP_LSE_BASE_2 = 0, 1
+DCP_F32, DCP_BF16 = 0, 1
+STATUS_BITS = {1: "BAD_POSITION", 2: "BAD_PAGE_INDEX", 4: "BAD_PAGE_ID", 8: "BAD_REQUEST", 16: "BAD_LENGTH"}
+
+
+class DcpError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed with {code} ({msg})")
+        self.code = code
+
+
+class Layout(ctypes.Structure):
+    """dcp_layout_t: n_shards N, interleave I (1 = token round-robin), page_size P."""
+    _fields_ = [("n_shards", ctypes.c_int32), ("interleave", ctypes.c_int32), ("page_size", ctypes.c_int32)]
+
+    def __repr__(self):
+        return f"Layout(N={self.n_shards}, I={self.interleave}, P={self.page_size})"
+
+
+_lib = None
+_c = ctypes
+_P = ctypes.c_void_p
+_I32, _I64, _SZ, _F = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_LP = ctypes.POINTER(Layout)
+
+_SIGNATURES = {
+    "dcp_version": (_I32, []),
+    "dcp_launch_count": (_I64, []),
+    "dcp_error_string": (ctypes.c_char_p, [_I32]),
+    "dcp_count": (_I64, [_LP, _I32, _I64]),
+    "dcp_slot_map": (_I32, [_LP, _P, _P, _I64, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "dcp_kv_append": (_I32, [_LP, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _P]),
+    "dcp_mla_decode_partial": (_I32, [_LP, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _I64, _I64,
+                                      _P, _F, _I32, _P, _I32, _P, _P, _SZ, _P, _P]),
+    "dcp_mla_decode_workspace_size": (_SZ, [_LP, _I32, _I32, _I32, _I32, _I32]),
+    "dcp_lse_merge": (_I32, [_I32, _I64, _P, _I32, _P, _I32, _P, _I32, _P, _P]),
+}
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load_library():
+    """Load libdcp_gb300.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != DCP_OK:
+        msg = load_library().dcp_error_string(code).decode()
+        raise DcpError(fn, code, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return DCP_F32
+    if t.dtype == torch.bfloat16:
+        return DCP_BF16
+    raise ValueError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def dcp_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().dcp_launch_count())
+
+
+def dcp_count(layout: Layout, shard: int, x: int) -> int:
+    """Positions in [0, x) owned by `shard` (host-only)."""
+    v = load_library().dcp_count(ctypes.byref(layout), shard, x)
+    if v < 0:
+        raise DcpError("dcp_count", DCP_ERR_INVALID, "invalid argument")
+    return int(v)
+
+
+def dcp_slot_map(layout, pos, req, block_table, max_pages, pool_pages, owner, row, slot, status, stream=None):
+    """(owner, local row, slot) of each new token; writes into owner/row/slot."""
+    T = pos.numel()
+    _dev(pos, "pos", torch.int64, (T,))
+    _dev(req, "req", torch.int32, (T,))
+    _dev(block_table, "block_table", torch.int32)
+    _dev(owner, "owner", torch.int32, (T,))
+    _dev(row, "row", torch.int64, (T,))
+    _dev(slot, "slot", torch.int64, (T,))
+    _dev(status, "status", torch.int32, (1,))
+    B, stride = block_table.shape
+    _check("dcp_slot_map", load_library().dcp_slot_map(
+        ctypes.byref(layout), _ptr(pos), _ptr(req), T, _ptr(block_table), B, stride, max_pages, pool_pages,
+        _ptr(owner), _ptr(row), _ptr(slot), _ptr(status), _stream(stream)))
+
+
+def dcp_kv_append(layout, shard_begin, shard_end, kv_new, owner, slot, arena, pool_pages, status, stream=None):
+    """Owner-filtered copy of kv_new [T, 576] bf16 into arena [shards, pool_pages*P, 576]."""
+    T = kv_new.shape[0]
+    _dev(kv_new, "kv_new", torch.bfloat16, (T, 576))
+    _dev(owner, "owner", torch.int32, (T,))
+    _dev(slot, "slot", torch.int64, (T,))
+    _dev(arena, "arena", torch.bfloat16, (shard_end - shard_begin, pool_pages * layout.page_size, 576))
+    _dev(status, "status", torch.int32, (1,))
+    _check("dcp_kv_append", load_library().dcp_kv_append(
+        ctypes.byref(layout), shard_begin, shard_end, _ptr(kv_new), _ptr(owner), _ptr(slot), T,
+        _ptr(arena), pool_pages, _ptr(status), _stream(stream)))
+
+
+def dcp_mla_decode_workspace_size(layout, shard_begin, shard_end, B, q_len, H) -> int:
+    return int(load_library().dcp_mla_decode_workspace_size(
+        ctypes.byref(layout), shard_begin, shard_end, B, q_len, H))
+
+
+def dcp_mla_decode_partial(layout, shard_begin, shard_end, q, arena, pool_pages, block_table, max_pages,
+                           seq_lens, scale, lse_base, o_part, lse_part, workspace, status, stream=None):
+    """Partials (o_r, lse_r) of shards [shard_begin, shard_end) for q [B, q_len, H, 576]."""
+    B, q_len, H, dk = q.shape
+    n = shard_end - shard_begin
+    _dev(q, "q", torch.bfloat16, (B, q_len, H, 576))
+    _dev(arena, "arena", torch.bfloat16, (n, pool_pages * layout.page_size, 576))
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int64, (B,))
+    _dev(o_part, "o_part", o_part.dtype, (n, B, q_len, H, 512))
+    _dev(lse_part, "lse_part", torch.float32, (n, B, q_len, H))
+    _dev(status, "status", torch.int32, (1,))
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _dev(workspace, "workspace", torch.uint8)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel()
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per request")
+    _check("dcp_mla_decode_partial", load_library().dcp_mla_decode_partial(
+        ctypes.byref(layout), shard_begin, shard_end, _ptr(q), B, q_len, H, _ptr(arena), pool_pages,
+        _ptr(block_table), block_table.shape[1], max_pages, _ptr(seq_lens), float(scale), lse_base,
+        _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), ws_ptr, ws_bytes, _ptr(status), _stream(stream)))
+
+
+def dcp_lse_merge(o_part, lse_part, lse_base, o, lse=None, stream=None):
+    """Merge o_part [n, rows, 512] / lse_part [n, rows] into o [rows, 512] / lse [rows]."""
+    n = o_part.shape[0]
+    rows = o_part.numel() // (n * 512) if n else 0
+    _dev(o_part, "o_part", o_part.dtype)
+    if o_part.shape[-1] != 512:
+        raise ValueError("o_part's last dim must be 512")
+    _dev(lse_part, "lse_part", torch.float32)
+    if lse_part.numel() != n * rows:
+        raise ValueError("lse_part must hold n_parts * rows values")
+    _dev(o, "o", o.dtype)
+    if o.numel() != rows * 512:
+        raise ValueError("o must hold rows * 512 values")
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+        if lse.numel() != rows:
+            raise ValueError("lse must hold rows values")
+    _check("dcp_lse_merge", load_library().dcp_lse_merge(
+        n, rows, _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), lse_base, _ptr(o), _dtype_code(o),
+        _ptr(lse), _stream(stream)))

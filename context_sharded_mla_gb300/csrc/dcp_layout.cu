@@ -1,0 +1,135 @@
+// dcp_layout.cu — slot map and owner-filtered append (integer / copy kernels).
+//
+// dcp_slot_map: one thread per new token computes (owner, local row, slot).
+// dcp_kv_append: one warp per new token copies its 1152-byte latent row with
+// 16-byte vector loads/stores into the owner's pool.  Both are tiny next to
+// the decode partial (B tokens per decode step; 8192 per chunk), so they are
+// written for latency: one launch each, no shared memory.
+#include "dcp_internal.cuh"
+
+#include <atomic>
+
+using namespace dcp;
+
+namespace dcp {
+static std::atomic<int64_t> g_launches{0};
+void note_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace dcp
+
+extern "C" int64_t dcp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" int32_t dcp_version(void) { return 10000; }
+
+extern "C" const char* dcp_error_string(int32_t code) {
+  switch (code) {
+    case DCP_OK: return "ok";
+    case DCP_ERR_INVALID: return "invalid argument";
+    case DCP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DCP_ERR_CUDA: return "CUDA call failed";
+    case DCP_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown error";
+  }
+}
+
+extern "C" int64_t dcp_count(const dcp_layout_t* layout, int32_t shard, int64_t x) {
+  if (!layout_ok(layout) || shard < 0 || shard >= layout->n_shards || x < 0) return -1;
+  return count_of(shard, x, to_layout(layout));
+}
+
+namespace {
+
+__global__ void slot_map_kernel(Layout L, const int64_t* __restrict__ pos,
+                                const int32_t* __restrict__ req, int64_t T,
+                                const int32_t* __restrict__ bt, int32_t B, int64_t bt_stride,
+                                int64_t max_pages, int64_t pool_pages, int32_t* __restrict__ owner,
+                                int64_t* __restrict__ row, int64_t* __restrict__ slot,
+                                int32_t* status) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int64_t p = pos[t];
+  const int32_t b = req[t];
+  int64_t own = -1, r = -1, s = -1;
+  if (p < 0) {
+    flag(status, DCP_STATUS_BAD_POSITION);
+  } else {
+    own = owner_of(p, L);
+    r = local_row_of(p, L);
+    const int64_t page_idx = r / L.P;
+    if (b < 0 || b >= B) {
+      flag(status, DCP_STATUS_BAD_REQUEST);
+    } else if (page_idx >= max_pages) {
+      flag(status, DCP_STATUS_BAD_PAGE_INDEX);
+    } else {
+      const int64_t page = bt[(int64_t)b * bt_stride + page_idx];
+      if (page < 0 || page >= pool_pages) {
+        flag(status, DCP_STATUS_BAD_PAGE_ID);
+      } else {
+        s = page * L.P + r % L.P;
+      }
+    }
+  }
+  owner[t] = (int32_t)own;
+  row[t] = r;
+  slot[t] = s;
+}
+
+// One warp per token; a 576-element bf16 row is 72 16-byte vectors.
+__global__ void kv_append_kernel(const uint4* __restrict__ kv_new, const int32_t* __restrict__ owner,
+                                 const int64_t* __restrict__ slot, int64_t T, uint4* __restrict__ arena,
+                                 int32_t shard_begin, int32_t shard_end, int64_t pool_rows,
+                                 int32_t* status) {
+  constexpr int kVec = kDk * 2 / 16;  // 72
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const int32_t own = owner[warp];
+  if (own < shard_begin || own >= shard_end) return;  // another device's shard
+  const int64_t s = slot[warp];
+  if (s < 0 || s >= pool_rows) {
+    if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_ID);
+    return;
+  }
+  const uint4* src = kv_new + warp * kVec;
+  uint4* dst = arena + ((int64_t)(own - shard_begin) * pool_rows + s) * kVec;
+  for (int i = lane; i < kVec; i += 32) dst[i] = __ldg(src + i);
+}
+
+}  // namespace
+
+extern "C" int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32_t* req,
+                                int64_t T, const int32_t* block_table, int32_t B, int64_t bt_stride,
+                                int64_t max_pages, int64_t pool_pages, int32_t* owner, int64_t* row,
+                                int64_t* slot, int32_t* status, void* stream) {
+  if (!layout_ok(layout) || T < 0 || B < 1 || max_pages < 1 || bt_stride < max_pages ||
+      pool_pages < 1)
+    return DCP_ERR_INVALID;
+  if (T == 0) return DCP_OK;
+  if (!pos || !req || !block_table || !owner || !row || !slot) return DCP_ERR_INVALID;
+  const int threads = 256;
+  const int64_t blocks = (T + threads - 1) / threads;
+  if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
+  slot_map_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(
+      to_layout(layout), pos, req, T, block_table, B, bt_stride, max_pages, pool_pages, owner, row,
+      slot, status);
+  return launch_status();
+}
+
+extern "C" int32_t dcp_kv_append(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                                 const void* kv_new, const int32_t* owner, const int64_t* slot,
+                                 int64_t T, void* arena, int64_t pool_pages, int32_t* status,
+                                 void* stream) {
+  if (!layout_ok(layout) || T < 0 || pool_pages < 1 || shard_begin < 0 ||
+      shard_end > layout->n_shards || shard_begin >= shard_end)
+    return DCP_ERR_INVALID;
+  if (T == 0) return DCP_OK;
+  if (!kv_new || !owner || !slot || !arena) return DCP_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(kv_new) | reinterpret_cast<uintptr_t>(arena)) & 15)
+    return DCP_ERR_INVALID;  // rows are moved as 16-byte vectors
+  const int threads = 256;  // 8 tokens per block
+  const int64_t blocks = (T * 32 + threads - 1) / threads;
+  if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
+  kv_append_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(
+      static_cast<const uint4*>(kv_new), owner, slot, T, static_cast<uint4*>(arena), shard_begin,
+      shard_end, pool_pages * layout->page_size, status);
+  return launch_status();
+}

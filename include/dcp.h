@@ -1,0 +1,230 @@
+/*
+ * dcp.h — C ABI of the sharded absorbed-MLA decode library (sm_103a / GB300).
+ *
+ * The library implements the data-parallel hot path of Decode Context
+ * Parallelism (DCP) for absorbed Multi-head Latent Attention:
+ *
+ *   1. dcp_slot_map            owner / local row / physical slot of each new token
+ *   2. dcp_kv_append           owner-filtered write of the 576-d latent rows
+ *   3. dcp_mla_decode_partial  per-shard partial attention (o_r, lse_r)
+ *   4. dcp_lse_merge           exact log-sum-exp merge of the N partials
+ *
+ * On one GPU the N context shards are N compact paged pools in one HBM
+ * allocation (the "arena"), so the cross-rank steps (query all-gather,
+ * all-to-all of the partials) become plain device buffers.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All pointers except `layout` and the host scalars are DEVICE pointers
+ *    (CUDA global memory of the current device).  The caller allocates and
+ *    frees every buffer; no call allocates device memory or keeps state
+ *    between calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls only enqueue work; they do not synchronise.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns DCP_ERR_INVALID (or DCP_ERR_UNSUPPORTED) and launches
+ *    nothing.  A failed launch returns DCP_ERR_CUDA.
+ *  - Data-dependent range errors found on the device (a negative position, a
+ *    local row past the block table, a page id outside the pool, a sequence
+ *    length the block table cannot hold) OR a DCP_STATUS_* bit into the
+ *    caller's device word `*status` and skip the offending read or write.
+ *    `status` is sticky: the library never clears it.  No kernel traps.
+ *  - bf16 means IEEE bfloat16 stored as 16-bit words; f32 is IEEE binary32.
+ *  - Tensors are dense and row-major ("C order") in the shapes given.
+ *
+ * Notation: N = layout->n_shards, I = layout->interleave (1 = token
+ * round-robin), P = layout->page_size (rows per physical page), Dk = 576
+ * latent dims (512 c_K + 64 k_R), Dv = 512 value dims (the c_K part).
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Shard layout.  Source: "PCP / DCP：计算、KV 布局与块轮转", section 6 (block
+ * round-robin with block size B, here `interleave`), and vLLM-Ascend
+ * "上下文并行（CP）", section "块表" (cp_kv_cache_interleave_size; the page size
+ * must be a multiple of it).  Requirements: n_shards >= 1, interleave >= 1,
+ * page_size >= 1 and page_size % interleave == 0. */
+typedef struct dcp_layout {
+  int32_t n_shards;
+  int32_t interleave;
+  int32_t page_size;
+} dcp_layout_t;
+
+/* Return codes. */
+enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID = -1,      /* bad argument (null pointer, size, layout, dtype) */
+  DCP_ERR_UNSUPPORTED = -2,  /* valid but outside what this build handles */
+  DCP_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed */
+  DCP_ERR_WORKSPACE = -4     /* workspace missing or smaller than required */
+};
+
+/* Device status bits (OR-ed into *status). */
+enum {
+  DCP_STATUS_BAD_POSITION = 1,    /* position < 0 */
+  DCP_STATUS_BAD_PAGE_INDEX = 2,  /* local row / P >= max_pages */
+  DCP_STATUS_BAD_PAGE_ID = 4,     /* block-table entry outside [0, pool_pages) */
+  DCP_STATUS_BAD_REQUEST = 8,     /* request index outside [0, B) */
+  DCP_STATUS_BAD_LENGTH = 16      /* seq_len < q_len */
+};
+
+enum { DCP_LSE_BASE_E = 0, DCP_LSE_BASE_2 = 1 };
+enum { DCP_F32 = 0, DCP_BF16 = 1 };
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t dcp_version(void);
+
+/* Short English description of a return code (static storage). */
+const char* dcp_error_string(int32_t code);
+
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all entry points, all devices).  Host-only; lets a caller count the
+ * library's launches inside a timed region. */
+int64_t dcp_launch_count(void);
+
+/*
+ * dcp_count — number of positions p in [0, x) owned by `shard`; host-only, pure.
+ *
+ * Source: "Decode Context Parallelism" (zdszero), section "Core abstraction",
+ * idea 1 (a chunk [a, a+L) gives a shard count(a+L) - count(a) positions), and
+ * "PCP / DCP：计算、KV 布局与块轮转", section 6, local_len:
+ *   count(x) = (x / (N*I)) * I + clamp(x % (N*I) - shard*I, 0, I).
+ * Returns -1 on a bad layout, shard outside [0, N) or x < 0.
+ */
+int64_t dcp_count(const dcp_layout_t* layout, int32_t shard, int64_t x);
+
+/*
+ * dcp_slot_map — placement of T new tokens.
+ *
+ * Sources: "Decode Context Parallelism" (zdszero), "Core abstraction" idea 1
+ * (owner(p) = p mod N, row(p) = floor(p / N)); "PCP / DCP：计算、KV 布局与块轮转"
+ * section 6 (owner = (p / I) % N, local row = (p / (N*I)) * I + p % I) and
+ * section "KV cache 管理" (slot = page_id * P + offset_in_page); SGLang
+ * "Decode context parallelism", "Virtual KV layout" (one shared block table;
+ * a widened page of N*P positions maps to one physical page on every shard).
+ *
+ *   pos          int64[T]  request-global positions (>= 0)
+ *   req          int32[T]  request index of each token, in [0, B)
+ *   block_table  int32[B, bt_stride]; entry [b][k] is the physical page (same
+ *                id on every shard) holding local rows [k*P, (k+1)*P) of b;
+ *                only columns k < max_pages are read
+ *   owner  (out) int32[T]  owning shard
+ *   row    (out) int64[T]  local row on the owner
+ *   slot   (out) int64[T]  row index inside the owner's pool = page * P + row % P,
+ *                          or -1 if the token could not be placed (status set)
+ *   status (in/out) int32 device word, see DCP_STATUS_*
+ * T == 0 is a no-op.  Errors: DCP_ERR_INVALID for a bad layout, T < 0,
+ * B < 1, max_pages < 1 or max_pages > bt_stride, or a null pointer with T > 0.
+ */
+int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32_t* req,
+                     int64_t T, const int32_t* block_table, int32_t B, int64_t bt_stride,
+                     int64_t max_pages, int64_t pool_pages, int32_t* owner, int64_t* row,
+                     int64_t* slot, int32_t* status, void* stream);
+
+/*
+ * dcp_kv_append — owner-filtered write of new latent rows.
+ *
+ * Source: "MLA 的 Decode Context Parallelism", section 4, stage 2 (every rank
+ * computes the new latent [c_K || k_R]; only the owner stores its row) and
+ * section 6 (set_mla_kv_buffer_dcp_sharded); "Decode Context Parallelism"
+ * (zdszero), SGLang K3 decode path (the new token's latent is written only to
+ * its owner rank).
+ *
+ *   kv_new  bf16[T, 576]  new latent rows
+ *   owner   int32[T], slot int64[T]: the output of dcp_slot_map
+ *   arena   bf16[shard_end - shard_begin, pool_pages * P, 576]: the pools of
+ *           shards [shard_begin, shard_end), one after another
+ * Token t is copied to arena[owner[t] - shard_begin][slot[t]] when
+ * shard_begin <= owner[t] < shard_end; tokens of other shards are skipped
+ * (another device holds them); slot < 0 or >= pool_pages * P is skipped and
+ * flagged DCP_STATUS_BAD_PAGE_ID.  Rows are copied bit for bit.
+ */
+int32_t dcp_kv_append(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                      const void* kv_new, const int32_t* owner, const int64_t* slot, int64_t T,
+                      void* arena, int64_t pool_pages, int32_t* status, void* stream);
+
+/*
+ * dcp_mla_decode_partial — locally normalised partial attention of each shard.
+ *
+ * Sources: "MLA 的 Decode Context Parallelism", section 2 (absorbed form:
+ * 576-d single-KV-head MQA, query per head [q_hat_C || q_R], value = c_K, the
+ * first 512 dims of the latent row) and section 3 (each rank returns o^(r) and
+ * lse_r); "Decode Context Parallelism" (zdszero), "Core abstraction" idea 2
+ * (O_r = softmax_local(q k^T * scale) V_r, L_r = log sum_{p in P_r} exp(s_p));
+ * "PCP / DCP：计算、KV 布局与块轮转" section 4.1 (an empty shard contributes a
+ * zero-weight state); SGLang "Decode context parallelism", "DCP x speculative
+ * decoding" (the verify kernel sees the shard rank and the GLOBAL lengths so the
+ * causal mask spans the whole sequence).
+ *
+ * For request b with S_b = seq_lens[b] cached tokens (the q_len new ones
+ * included), query token t sits at position S_b - q_len + t and sees every
+ * position p <= S_b - q_len + t.  For each held shard r, query token t and
+ * head h, with V_r the visible positions owned by r:
+ *   s_p     = scale * sum_{d<576} q[b,t,h,d] * k_p[d]
+ *   lse_r   = ln sum_{p in V_r} exp(s_p)      (log2 of the same sum if lse_base == 1)
+ *   o_r     = sum_{p in V_r} exp(s_p - lse_e) * k_p[0:512]
+ *   V_r empty -> lse_r = -inf, o_r = 0.
+ *
+ *   q          bf16[B, q_len, H, 576]
+ *   arena      bf16[shard_end - shard_begin, pool_pages * P, 576]
+ *   block_table, bt_stride, max_pages: as for dcp_slot_map
+ *   seq_lens   int64[B] (device)
+ *   o_part     [shard_end - shard_begin, B, q_len, H, 512], f32 or bf16 (o_part_dtype)
+ *   lse_part   f32[shard_end - shard_begin, B, q_len, H]
+ *   workspace  device scratch of at least dcp_mla_decode_workspace_size(...)
+ *              bytes, 256-byte aligned; its contents need not be initialised
+ *              and are meaningless after the call
+ * Rows of a page past the request's length are read but carry zero weight;
+ * they must hold finite values (a zero-initialised pool and dcp_kv_append
+ * guarantee that).  Supported: 1 <= H, q_len * H <= 1024, B >= 1.
+ * Errors: DCP_ERR_INVALID on bad sizes/pointers/dtype/base, DCP_ERR_WORKSPACE
+ * if the workspace is too small.  Device status: BAD_LENGTH, BAD_PAGE_ID.
+ */
+int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                               const void* q, int32_t B, int32_t q_len, int32_t H,
+                               const void* arena, int64_t pool_pages,
+                               const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                               const int64_t* seq_lens, float scale, int32_t lse_base,
+                               void* o_part, int32_t o_part_dtype, float* lse_part,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* status, void* stream);
+
+/* Workspace bytes dcp_mla_decode_partial needs for these sizes on the current
+ * device (0 on bad arguments).  It does not depend on the sequence lengths. */
+size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int32_t shard_begin,
+                                     int32_t shard_end, int32_t B, int32_t q_len, int32_t H);
+
+/*
+ * dcp_lse_merge — exact merge of n_parts partials per row.
+ *
+ * Sources: "Decode Context Parallelism" (zdszero), "Theory": merge identity
+ * O = sum_r exp(L_r) O_r / sum_r exp(L_r), its stable form with m = max_r L_r,
+ * L = m + log sum_r exp(L_r - m), and the rule that exp/log must match the
+ * base the kernel reported; "MLA 的 Decode Context Parallelism", section 3
+ * (w_r = exp2(lse_r - m), out = sum_r w_r o^(r) / sum_r w_r); SGLang "Decode
+ * context parallelism", "MLA decode dataflow" (lse = logsumexp_r lse_r,
+ * o = sum_r exp(lse_r - lse) o_r, base e or base 2).
+ *
+ *   o_part   [n_parts, rows, 512] f32 or bf16 (o_part_dtype)
+ *   lse_part f32[n_parts, rows], in base e (lse_base 0) or base 2 (lse_base 1)
+ *   o        [rows, 512] f32 or bf16 (o_dtype)
+ *   lse      f32[rows] in the same base (may be NULL if not wanted)
+ * A part with lse = -inf has zero weight; a row whose parts are all -inf gets
+ * o = 0 and lse = -inf.  rows == 0 is a no-op.  Errors: DCP_ERR_INVALID.
+ */
+int32_t dcp_lse_merge(int32_t n_parts, int64_t rows, const void* o_part, int32_t o_part_dtype,
+                      const float* lse_part, int32_t lse_base, void* o, int32_t o_dtype,
+                      float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads and exports every symbol include/dcp.h declares (no GPU).
+
+Also checks the host-only parts: dcp_count against the oracle, and that bad
+arguments are rejected on the host before anything is launched.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import layout as olayout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from context_sharded_mla_gb300 import _build, load_library
+    _build.build()
+    return load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dcp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dcp_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
+              "dcp_mla_decode_workspace_size", "dcp_lse_merge"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/dcp.h but not exported"
+
+
+def test_version_and_errors(lib):
+    assert lib.dcp_version() >= 10000
+    assert lib.dcp_error_string(-1) == b"invalid argument"
+    assert lib.dcp_error_string(0) == b"ok"
+
+
+@pytest.mark.parametrize("N,I", [(1, 1), (4, 1), (8, 1), (16, 16), (4, 4), (3, 2)])
+def test_dcp_count_matches_oracle(lib, N, I):
+    from context_sharded_mla_gb300 import Layout, dcp_count
+    lay = Layout(N, I, I * 4)
+    for r in range(N):
+        for x in list(range(0, 5 * N * I)) + [10**6 + 3, 2**40 + 17]:
+            assert dcp_count(lay, r, x) == int(olayout.count(r, x, N, I))
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    from context_sharded_mla_gb300 import Layout
+    bad = Layout(4, 3, 16)          # interleave does not divide the page
+    good = Layout(4, 1, 16)
+    P = ctypes.c_void_p
+    assert lib.dcp_count(ctypes.byref(bad), 0, 5) == -1
+    assert lib.dcp_count(ctypes.byref(good), 4, 5) == -1
+    assert lib.dcp_count(ctypes.byref(good), 0, -1) == -1
+    assert lib.dcp_slot_map(ctypes.byref(bad), P(16), P(16), 1, P(16), 1, 1, 1, 1, P(16), P(16), P(16),
+                            P(16), None) == -1
+    assert lib.dcp_slot_map(ctypes.byref(good), P(16), P(16), 0, P(16), 1, 1, 1, 1, P(16), P(16), P(16),
+                            P(16), None) == 0       # T == 0 is a no-op
+    assert lib.dcp_kv_append(ctypes.byref(good), 0, 5, P(16), P(16), P(16), 1, P(16), 1, P(16), None) == -1
+    assert lib.dcp_kv_append(ctypes.byref(good), 0, 4, P(17), P(16), P(16), 1, P(16), 1, P(16), None) == -1
+    # decode: H*q_len over the limit, bad base, bad dtype, missing workspace
+    args = lambda **kw: dict(dict(sb=0, se=4, q=P(256), B=1, ql=1, H=16, ar=P(256), pp=1, bt=P(256), st=1, mp=1,
+                                  sl=P(256), sc=0.1, base=0, op=P(256), od=0, lp=P(256), ws=None, wsb=0,
+                                  status=P(256)), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return lib.dcp_mla_decode_partial(ctypes.byref(good), a["sb"], a["se"], a["q"], a["B"], a["ql"], a["H"],
+                                          a["ar"], a["pp"], a["bt"], a["st"], a["mp"], a["sl"], a["sc"], a["base"],
+                                          a["op"], a["od"], a["lp"], a["ws"], a["wsb"], a["status"], None)
+    assert call(H=2048) == -1
+    assert call(base=7) == -1
+    assert call(od=9) == -1
+    assert call(sc=-1.0) == -1
+    assert call(se=5) == -1
+    assert call(q=None) == -1
+    assert call(mp=2, st=1) == -1
+    need = lib.dcp_mla_decode_workspace_size(ctypes.byref(good), 0, 4, 1, 1, 16)
+    if need > 0:
+        assert call(wsb=need - 1, ws=P(256)) == -4
+    # merge
+    assert lib.dcp_lse_merge(0, 10, P(256), 0, P(256), 0, P(256), 0, P(256), None) == -1
+    assert lib.dcp_lse_merge(2, 10, P(256), 3, P(256), 0, P(256), 0, P(256), None) == -1
+    assert lib.dcp_lse_merge(2, 0, None, 0, None, 0, None, 0, None, None) == 0
+
+
+def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
+    import context_sharded_mla_gb300 as dcp
+    monkeypatch.setattr(dcp, "_lib", None)
+    monkeypatch.setattr(dcp._build, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        dcp.load_library()
