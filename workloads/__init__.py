@@ -144,10 +144,10 @@ def gen_kv(cfg: Config, b: int, S_b: int, device="cpu") -> torch.Tensor:
 
 
 def needle_positions(cfg: Config, S_b: torch.Tensor) -> torch.Tensor:
-    """One seeded position per request where a planted 'needle' row is placed."""
+    """One seeded position per request for a planted 'needle' row (visible to every query token)."""
     g = torch.Generator().manual_seed(cfg.seed * 31337 + 5)
     u = torch.rand(cfg.B, generator=g, dtype=torch.float64)
-    return torch.clamp((u * S_b.to(torch.float64)).to(torch.int64), max=S_b - 1)
+    return torch.clamp((u * S_b.to(torch.float64)).to(torch.int64), min=0, max=S_b - cfg.q_len)
 
 
 def plant_needle(q: torch.Tensor, kv_b: torch.Tensor, b: int, p: int, head: int = 0):
