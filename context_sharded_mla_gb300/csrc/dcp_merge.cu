@@ -7,8 +7,8 @@
 // out = sum_r w_r o_r / sum_r w_r.
 //
 // One warp per output row.  Every lane owns 16 of the 512 value dims, read as
-// 16-byte vectors so that each warp access is one contiguous 512-byte (f32) or
-// 256-byte (bf16) segment per part.  Algorithmic bytes per row:
+// 16-byte vectors so that each warp access is one contiguous 1024-byte (f32) or
+// 512-byte (bf16) segment per part.  Algorithmic bytes per row:
 // n_parts * (512 * sizeof(o_part) + 4) read, 512 * sizeof(o) + 4 written.
 #include "dcp_internal.cuh"
 
@@ -16,6 +16,8 @@ using namespace dcp;
 
 namespace {
 
+// Lane l owns the 16 dims [8l, 8l+8) and [256 + 8l, 256 + 8l + 8) in every
+// dtype, so the f32 and bf16 paths agree on which lane holds which dim.
 template <int kInBf16>
 __device__ inline void load16(const void* base, int64_t row, int lane, float (&v)[16]) {
   if (kInBf16) {
@@ -34,9 +36,11 @@ __device__ inline void load16(const void* base, int64_t row, int lane, float (&v
   } else {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kDv);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float4 f = __ldg(p + lane + 32 * j);
-      v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+    for (int j = 0; j < 2; ++j) {
+      float4 a = __ldg(p + 2 * lane + 64 * j);
+      float4 b = __ldg(p + 2 * lane + 64 * j + 1);
+      v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = a.z; v[8 * j + 3] = a.w;
+      v[8 * j + 4] = b.x; v[8 * j + 5] = b.y; v[8 * j + 6] = b.z; v[8 * j + 7] = b.w;
     }
   }
 }
@@ -56,8 +60,10 @@ __device__ inline void store16(void* base, int64_t row, int lane, const float (&
   } else {
     float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + row * kDv);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      p[lane + 32 * j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int j = 0; j < 2; ++j) {
+      p[2 * lane + 64 * j] = make_float4(v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3]);
+      p[2 * lane + 64 * j + 1] = make_float4(v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
+    }
   }
 }
 

@@ -147,7 +147,8 @@ def needle_positions(cfg: Config, S_b: torch.Tensor) -> torch.Tensor:
     """One seeded position per request for a planted 'needle' row (visible to every query token)."""
     g = torch.Generator().manual_seed(cfg.seed * 31337 + 5)
     u = torch.rand(cfg.B, generator=g, dtype=torch.float64)
-    return torch.clamp((u * S_b.to(torch.float64)).to(torch.int64), min=0, max=S_b - cfg.q_len)
+    p = (u * S_b.to(torch.float64)).to(torch.int64)
+    return torch.clamp(torch.minimum(p, S_b - cfg.q_len), min=0)
 
 
 def plant_needle(q: torch.Tensor, kv_b: torch.Tensor, b: int, p: int, head: int = 0):
