@@ -31,7 +31,8 @@ __all__ = [
 DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA, DCP_ERR_WORKSPACE = 0, -1, -2, -3, -4
 DCP_LSE_BASE_E, DCP_LSE_BASE_2 = 0, 1
 DCP_F32, DCP_BF16 = 0, 1
-STATUS_BITS = {1: "BAD_POSITION", 2: "BAD_PAGE_INDEX", 4: "BAD_PAGE_ID", 8: "BAD_REQUEST", 16: "BAD_LENGTH"}
+STATUS_BITS = {1: "BAD_POSITION", 2: "BAD_PAGE_INDEX", 4: "BAD_PAGE_ID", 8: "BAD_REQUEST", 16: "BAD_LENGTH",
+               32: "TIMEOUT"}
 
 
 class DcpError(RuntimeError):

@@ -1,192 +1,748 @@
-// dcp_decode.cu — per-shard partial attention (o_r, lse_r) for absorbed MLA.
+// dcp_decode.cu — per-shard partial attention (o_r, lse_r) for absorbed MLA on sm_103a.
 //
 // Sources: "MLA 的 Decode Context Parallelism", section 2 (absorbed form: one
 // 576-d KV head shared by all query heads; values are the first 512 dims) and
 // section 3 (each rank returns its locally normalised output and its LSE);
-// "Decode Context Parallelism" (zdszero), "Core abstraction" idea 2;
-// SGLang "Decode context parallelism", "DCP x speculative decoding" (causal
-// mask in global positions, from the shard rank and the global lengths).
+// "Decode Context Parallelism" (zdszero), "Core abstraction" idea 2 and
+// "Theory" (the (Z, N) merge operator: a shard may itself be split into pieces
+// that are merged the same way); SGLang "Decode context parallelism",
+// "DCP x speculative decoding" (causal mask in global positions, from the shard
+// rank and the global lengths).
 //
-// First version: a plain SIMT kernel, one CTA per (16 query rows, shard,
-// request), streaming the shard's rows through shared memory in tiles of 32
-// with an online (running max / running sum) softmax.  Visible local rows of
-// query row (t, h): [0, count_r(S_b - q_len + t + 1)).
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: query rows once per segment; KV tiles of 64 local
+//               rows x 64 dims ("chunks", 8 KB, 128-byte swizzle) into a ring.
+//   warp 1      tcgen05 issuer (one thread) and TMEM owner.
+//   warps 2-5   softmax (one query row per thread) and epilogue.
+// Per KV tile j of 64 rows:
+//   S_j   = Q K_j^T            M=128 query rows (R_g valid), N=64 rows, K=576   (TMEM, fp32)
+//   P_j   = exp2(S_j*scale*log2e - m)      online softmax with lazy rescaling
+//   O^T  += V_j^T P_j^T        M=128 value dims (x4 tiles), N=R_g rows, K=64  (TMEM, fp32)
+// O is kept transposed (dims on TMEM lanes, query rows on columns) so that 4*R_g
+// columns of fp32 accumulator plus two 64-column S buffers fit in 512 columns.
+// The tile's V chunks are fetched a second time for the PV product (from L2)
+// because the 576-d K pass and the query block leave no room to keep a tile.
+//
+// Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
+// concatenation of all units' tiles is cut into V equal ranges, one per CTA (or
+// per group of CTAs when the query rows need several row groups).  A unit that
+// lies inside one range is written directly; a unit cut by range boundaries
+// leaves normalised pieces (o, lse in base 2) in the workspace which a second
+// kernel merges with the same LSE rule.  A third tiny kernel (run first) writes
+// the tile prefix sums.
+#include <cudaTypedefs.h>
+
 #include "dcp_internal.cuh"
+#include "sm100_ptx.cuh"
 
 using namespace dcp;
+using namespace dcp::sm100;
 
 namespace {
 
-constexpr int kRowsPerCta = 16;
-constexpr int kTile = 32;
-constexpr int kKvPitch = kDk + 8;  // bf16 elements; 1168-byte rows stay 16-byte aligned
+constexpr int kTile = 64;          // KV rows per tile
+constexpr int kChunkDims = 64;     // dims per chunk (one 128-byte swizzle row)
+constexpr int kNumChunks = 9;      // 576 / 64
+constexpr int kChunkBytes = kTile * 128;
+constexpr int kKSlots = 10;        // ring uses per K pass (9 chunks + 1 unused, keeps V pairs aligned)
+constexpr int kVSlots = 8;         // ring uses per V pass (chunks 0..7)
+constexpr int kMaxSlots = 24;
+constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
+constexpr int kMaxGroupRows = 96;
 
-struct PartialArgs {
+struct TcArgs {
   Layout L;
-  int32_t shard_begin;
-  const __nv_bfloat16* q;
-  int32_t B, q_len, H;
-  const __nv_bfloat16* arena;
-  int64_t pool_rows;
-  int64_t pool_pages;
+  int32_t shard_begin, n_held;
+  int32_t B, q_len, H, R_total;  // R_total = q_len * H
+  int32_t Rg, ngroups, V;        // rows per group, groups, stream-K ranges
+  int32_t nslot;
+  int32_t box_rows;              // KV TMA box height = min(P, 64)
+  int64_t pool_rows, pool_pages;
   const int32_t* bt;
   int64_t bt_stride, max_pages;
   const int64_t* seq_lens;
-  float scale_log2;  // scale * log2(e): scores are kept in base 2
+  float scale_log2;
   int32_t base2;
   void* o_part;
   int32_t o_bf16;
   float* lse_part;
+  const int32_t* tile_start;  // [U + 1]
+  float* piece_o;             // [2V][R_total][512]
+  float* piece_lse;           // [2V][R_total]
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(256) partial_simt_kernel(PartialArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  float* q_s = reinterpret_cast<float*>(smem);                                       // [16][576]
-  __nv_bfloat16* kv_s = reinterpret_cast<__nv_bfloat16*>(q_s + kRowsPerCta * kDk);  // [32][580]
-  __shared__ int64_t nvis_s[kRowsPerCta];
+struct SmemLayout {
+  uint32_t q, ring, p, alpha, inv, vote, bars, misc, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int Rg, int nslot) {
+  SmemLayout s;
+  s.q = 0;
+  s.ring = kNumChunks * Rg * 128;
+  s.p = s.ring + nslot * kChunkBytes;
+  s.alpha = s.p + 2 * Rg * 128;
+  s.inv = s.alpha + 2 * 128 * 4;
+  s.vote = s.inv + 2 * 128 * 4;
+  s.bars = s.vote + 64;
+  s.misc = s.bars + (2 * kMaxSlots + 16) * 8;
+  s.total = s.misc + 64;
+  return s;
+}
+
+enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPFree0, kPFree1, kOFree,
+           kGroup, kNumFixedBars };
+
+__device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
+  const int64_t S = a.seq_lens[b];
+  if (S < a.q_len) {
+    *bad = true;
+    return 0;
+  }
+  return count_of(a.shard_begin + rs, S, a.L);
+}
+
+// ---------------------------------------------------------------------------- planner
+__global__ void __launch_bounds__(1024) plan_kernel(TcArgs a, int32_t* tile_start, int32_t U) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int32_t base = 0; base < U; base += 1024) {
+    const int32_t u = base + threadIdx.x;
+    int32_t t = 0;
+    if (u < U) {
+      bool bad = false;
+      const int b = u / a.n_held, rs = u % a.n_held;
+      const int64_t n = unit_nvis_max(a, b, rs, &bad);
+      if (bad && rs == 0) flag(a.status, DCP_STATUS_BAD_LENGTH);
+      t = (int32_t)((n + kTile - 1) / kTile);
+    }
+    // block-wide inclusive scan
+    int32_t x = t;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, x, s);
+      if (lane >= s) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int32_t ws = warp_sums[lane];
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, ws, s);
+        if (lane >= s) ws += y;
+      }
+      warp_sums[lane] = ws;
+    }
+    __syncthreads();
+    const int32_t incl = x + (w > 0 ? warp_sums[w - 1] : 0) + carry;
+    if (u < U) tile_start[u] = incl - t;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) tile_start[U] = carry;
+}
+
+// ---------------------------------------------------------------------------- segments
+// A CTA's range [lo, hi) of the global tile sequence, visited unit by unit.
+struct SegIter {
+  const int32_t* start;
+  int32_t U;
+  int64_t lo, hi;
+  int32_t u;
+
+  __device__ void init(const int32_t* st, int32_t nunits, int64_t lo_, int64_t hi_) {
+    start = st; U = nunits; lo = lo_; hi = hi_;
+    // largest u with start[u] <= lo
+    int32_t l = 0, h = U;  // start[U] = total > lo when lo < hi
+    while (h - l > 1) {
+      const int32_t m = (l + h) >> 1;
+      if (start[m] <= lo) l = m; else h = m;
+    }
+    u = l;
+  }
+  // next segment: unit, first tile (within the unit), tile count, whole-unit flag, piece slot
+  __device__ bool next(int32_t* unit, int32_t* t0, int32_t* nt, bool* whole, int* kslot) {
+    while (u < U) {
+      const int64_t s = start[u], e = start[u + 1];
+      if (s >= hi) return false;
+      const int64_t a = s > lo ? s : lo, b = e < hi ? e : hi;
+      const int32_t cur = u++;
+      if (a < b) {
+        *unit = cur;
+        *t0 = (int32_t)(a - s);
+        *nt = (int32_t)(b - a);
+        *whole = (a == s) && (b == e);
+        *kslot = (a == lo) ? 0 : 1;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+__device__ inline int64_t range_lo(int64_t T, int v, int V) { return (T * v) / V; }
+
+// ---------------------------------------------------------------------------- main kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
+                      TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemLayout sl = smem_layout(a.Rg, a.nslot);
+  unsigned char* q_s = smem + sl.q;
+  unsigned char* ring = smem + sl.ring;
+  unsigned char* p_s = smem + sl.p;
+  float* alpha_s = reinterpret_cast<float*>(smem + sl.alpha);  // [2][128]
+  float* inv_s = reinterpret_cast<float*>(smem + sl.inv);      // [2][128]
+  volatile int* vote_s = reinterpret_cast<volatile int*>(smem + sl.vote);  // [2][4]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
+  uint64_t* full = bars + kNumFixedBars;
+  uint64_t* empty = full + kMaxSlots;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + sl.misc);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + sl.misc + 4);
 
   const int tid = threadIdx.x;
-  const int i = tid >> 4;   // row within the CTA
-  const int j = tid & 15;   // lane within the row group
-  const int R = a.q_len * a.H;
-  const int row0 = blockIdx.x * kRowsPerCta;
-  const int rs = blockIdx.y;              // held-shard index
-  const int64_t r = a.shard_begin + rs;   // global shard id
-  const int b = blockIdx.z;
-  const int64_t S = a.seq_lens[b];
-  const bool bad_len = S < a.q_len;
-  if (bad_len && tid == 0) flag(a.status, DCP_STATUS_BAD_LENGTH);
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int v = blockIdx.x / a.ngroups;
+  const int g = blockIdx.x % a.ngroups;
+  const int Rg = a.Rg;
+  const int nslot = a.nslot;
+  const int32_t U = a.B * a.n_held;
 
-  // query rows -> fp32 in shared memory; visible-row count per query row
-  for (int e = tid; e < kRowsPerCta * kDk; e += blockDim.x) {
-    const int ri = e / kDk, d = e % kDk;
-    const int row = row0 + ri;
-    float v = 0.f;
-    if (row < R) v = __bfloat162float(a.q[((int64_t)b * R + row) * kDk + d]);
-    q_s[e] = v;
-  }
-  if (tid < kRowsPerCta) {
-    const int row = row0 + tid;
-    int64_t nv = 0;
-    if (row < R && !bad_len) {
-      const int t = row / a.H;
-      nv = count_of(r, S - a.q_len + t + 1, a.L);
+  if (tid == 0) {
+    *abort_s = 0;
+    for (int i = 0; i < kNumFixedBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[kSFree0], 4);
+    mbar_init(&bars[kSFree1], 4);
+    mbar_init(&bars[kPFull0], 4);
+    mbar_init(&bars[kPFull1], 4);
+    mbar_init(&bars[kOFree], 4);
+    mbar_init(&bars[kGroup], 4);
+    for (int i = 0; i < nslot; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    nvis_s[tid] = nv;
+    fence_barrier_init();
   }
+  // stale ring rows past a request's last page are read (with zero weight):
+  // start from finite zeros
+  for (int i = tid; i < nslot * kChunkBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  int64_t n_max = 0;
-  for (int k = 0; k < kRowsPerCta; ++k) n_max = max(n_max, nvis_s[k]);
-  const int64_t my_nvis = nvis_s[i];
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
 
-  float m = -INFINITY;  // running max (base-2 units)
-  float l = 0.f;        // running sum of exp2(s - m)
-  float acc[32];        // dims 2*(j + 16k) and +1, k = 0..15
-#pragma unroll
-  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+  const int64_t T = a.tile_start[U];
+  const int64_t lo = range_lo(T, v, a.V), hi = range_lo(T, v + 1, a.V);
 
-  const __nv_bfloat16* pool = a.arena + (int64_t)rs * a.pool_rows * kDk;
-  const int32_t* bt_b = a.bt + (int64_t)b * a.bt_stride;
-
-  for (int64_t rho0 = 0; rho0 < n_max; rho0 += kTile) {
-    __syncthreads();
-    // gather 32 local rows through the block table (16-byte vectors)
-    for (int e = tid; e < kTile * (kDk / 8); e += blockDim.x) {
-      const int tr = e / (kDk / 8), c = e % (kDk / 8);
-      const int64_t rho = rho0 + tr;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (rho < n_max) {
-        const int64_t pidx = rho / a.L.P;
-        const int64_t page = pidx < a.max_pages ? (int64_t)bt_b[pidx] : -1;
-        if (page >= 0 && page < a.pool_pages) {
-          v = __ldg(reinterpret_cast<const uint4*>(pool + (page * a.L.P + rho % a.L.P) * kDk) + c);
-        } else if (c == 0) {
-          flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0 && lo < hi) {
+      prefetch_tmap(&tmap_q);
+      prefetch_tmap(&tmap_kv);
+      SegIter it;
+      it.init(a.tile_start, U, lo, hi);
+      int32_t u, t0, nt, kslot;
+      bool whole;
+      uint32_t use = 0;  // ring uses so far
+      int seg = 0;
+      bool ok = true;
+      auto load_pass = [&](int b, int rs, int64_t nvis, int32_t tile, bool kpass) -> bool {
+        const int64_t rho0 = (int64_t)tile * kTile;
+        const int nchunks = kpass ? kNumChunks : kVSlots;
+        const int nuses = kpass ? kKSlots : kVSlots;
+        for (int k = 0; k < nuses; ++k) {
+          const uint32_t slot = use % nslot;
+          const uint32_t round = use / nslot;
+          if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_s)) return false;
+          unsigned char* dst = ring + slot * kChunkBytes;
+          if (k >= nchunks) {
+            mbar_arrive(&full[slot]);
+          } else {
+            // boxes of box_rows rows covering local rows [rho0, rho0 + 64)
+            int nbox = kTile / a.box_rows;
+            uint32_t bytes = 0;
+            int64_t ys[kTile / 8];
+            int nvalid = 0;
+            for (int q = 0; q < nbox; ++q) {
+              const int64_t rho = rho0 + (int64_t)q * a.box_rows;
+              ys[q] = -1;
+              if (rho >= nvis) continue;
+              const int64_t pidx = rho / a.L.P;
+              int64_t page = pidx < a.max_pages ? (int64_t)a.bt[(int64_t)b * a.bt_stride + pidx] : -1;
+              if (page < 0 || page >= a.pool_pages) {
+                flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+                continue;
+              }
+              ys[q] = (int64_t)rs * a.pool_rows + page * a.L.P + rho % a.L.P;
+              bytes += a.box_rows * 128;
+              ++nvalid;
+            }
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            for (int q = 0; q < nbox; ++q)
+              if (ys[q] >= 0)
+                tma_load_2d(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, (int32_t)ys[q]);
+          }
+          ++use;
+        }
+        return true;
+      };
+      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+        const int b = u / a.n_held, rs = u % a.n_held;
+        bool bad = false;
+        const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
+        if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars[kQFull], kNumChunks * Rg * 128);
+        const int32_t qrow = b * a.R_total + g * Rg;
+        for (int k = 0; k < kNumChunks; ++k)
+          tma_load_2d(q_s + k * Rg * 128, &tmap_q, &bars[kQFull], k * kChunkDims, qrow);
+        ++seg;
+        for (int jj = 0; jj < nt && ok; ++jj) {
+          ok = load_pass(b, rs, nvis, t0 + jj, true);
+          if (ok && jj >= 1) ok = load_pass(b, rs, nvis, t0 + jj - 1, false);
+        }
+        if (ok) ok = load_pass(b, rs, nvis, t0 + nt - 1, false);
+      }
+      if (!ok) {
+        // drain: wait (bounded, ignoring the abort flag) for copies already issued
+        for (uint32_t k = 0; k < (uint32_t)nslot && k < use; ++k) {
+          const uint32_t uu = use - 1 - k;
+          const uint32_t slot = uu % nslot;
+          const uint64_t t0n = globaltimer();
+          while (!mbar_try_wait(&full[slot], (uu / nslot) & 1) && globaltimer() - t0n < kWaitLimitNs) {
+          }
+        }
+        const uint64_t t0n = globaltimer();
+        while (!mbar_try_wait(&bars[kQFull], (seg - 1) & 1) && seg > 0 && globaltimer() - t0n < kWaitLimitNs) {
         }
       }
-      *reinterpret_cast<uint4*>(kv_s + tr * kKvPitch + c * 8) = v;
     }
-    __syncthreads();
-    // scores of tokens j and j+16 for row i
-    float s[2];
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && lo < hi) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, Rg, 1, 0);
+      const uint32_t q_addr = smem_u32(q_s);
+      const uint32_t ring_addr = smem_u32(ring);
+      const uint32_t p_addr = smem_u32(p_s);
+      SegIter it;
+      it.init(a.tile_start, U, lo, hi);
+      int32_t u, t0, nt, kslot;
+      bool whole;
+      uint32_t use = 0;
+      uint32_t jglob = 0;  // tiles started by this CTA
+      int seg = 0;
+      bool ok = true;
+      auto qk = [&](uint32_t j) -> bool {
+        const int sb = j & 1;
+        if (!mbar_wait(&bars[kSFree0 + sb], ((j >> 1) & 1) ^ 1, abort_s)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + 4 * Rg + kTile * sb;
+        for (int k = 0; k < kKSlots; ++k) {
+          const uint32_t slot = use % nslot, round = use / nslot;
+          if (!mbar_wait(&full[slot], round & 1, abort_s)) return false;
+          if (k < kNumChunks) {
+            tc_fence_after();
+            const uint32_t kaddr = ring_addr + slot * kChunkBytes;
+            const uint32_t qaddr = q_addr + k * Rg * 128;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int tok = j + 16 * u;
-      const __nv_bfloat162* kr = reinterpret_cast<const __nv_bfloat162*>(kv_s + tok * kKvPitch);
-      const float2* qr = reinterpret_cast<const float2*>(q_s + i * kDk);
-      float dot = 0.f;
-#pragma unroll 8
-      for (int d2 = 0; d2 < kDk / 2; ++d2) {
-        const float2 kf = __bfloat1622float2(kr[d2]);
-        const float2 qf = qr[d2];
-        dot = fmaf(qf.x, kf.x, dot);
-        dot = fmaf(qf.y, kf.y, dot);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(d, sw128_desc(qaddr + kk * 32, 16, 1024), sw128_desc(kaddr + kk * 32, 16, 1024), idesc_qk,
+                          (k | kk) != 0);
+            mma_commit(&empty[slot]);
+          } else {
+            mbar_arrive(&empty[slot]);
+          }
+          ++use;
+        }
+        mma_commit(&bars[kSFull0 + sb]);
+        return true;
+      };
+      auto pv = [&](uint32_t j, bool first) -> bool {
+        const int pb = j & 1;
+        if (!mbar_wait(&bars[kPFull0 + pb], (j >> 1) & 1, abort_s)) return false;
+        if (first && seg >= 2) {
+          if (!mbar_wait(&bars[kOFree], (seg - 2) & 1, abort_s)) return false;
+        }
+        tc_fence_after();
+        const uint32_t pbase = p_addr + pb * Rg * 128;
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t slot = use % nslot, round = use / nslot;
+          const uint32_t slot2 = (use + 1) % nslot, round2 = (use + 1) / nslot;
+          if (!mbar_wait(&full[slot], round & 1, abort_s)) return false;
+          if (!mbar_wait(&full[slot2], round2 & 1, abort_s)) return false;
+          tc_fence_after();
+          const uint32_t vaddr = ring_addr + slot * kChunkBytes;
+          const uint32_t d = tmem + t * Rg;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, sw128_desc(vaddr + kk * 2048, kChunkBytes, 1024), sw128_desc(pbase + kk * 32, 16, 1024),
+                        idesc_pv, !(first && kk == 0));
+          mma_commit(&empty[slot]);
+          mma_commit(&empty[slot2]);
+          use += 2;
+        }
+        mma_commit(&bars[kPFree0 + pb]);
+        return true;
+      };
+      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+        if (!mbar_wait(&bars[kQFull], seg & 1, abort_s)) { ok = false; break; }
+        ++seg;
+        const uint32_t jfirst = jglob;
+        for (int jj = 0; jj < nt && ok; ++jj) {
+          ok = qk(jglob);
+          if (ok && jj == nt - 1) mma_commit(&bars[kQEmpty]);
+          if (ok && jj >= 1) ok = pv(jglob - 1, jglob - 1 == jfirst);
+          ++jglob;
+        }
+        if (ok) ok = pv(jglob - 1, jglob - 1 == jfirst);
       }
-      s[u] = (rho0 + tok < my_nvis) ? dot * a.scale_log2 : -INFINITY;
     }
-    float tmax = fmaxf(s[0], s[1]);
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    // All waits here are warp-uniform (every lane waits, then __all_sync), and the
+    // four warps meet only through the bounded kGroup mbarrier, so a timeout
+    // anywhere drains every thread instead of stranding some at a barrier.
+    const int c = 32 * (warp & 3) + lane;        // TMEM lane: query row (S) / value dim (O^T)
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    if (lo < hi) {
+      auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool r = mbar_wait(bar, parity, abort_s);
+        return __all_sync(0xffffffffu, r);
+      };
+      uint32_t gphase = 0;  // kGroup phases passed
+      // every softmax warp arrives; returns the OR of the warps' flags
+      auto group_sync = [&](bool flag_in, bool* any) -> bool {
+        const bool wany = __any_sync(0xffffffffu, flag_in);
+        if (lane == 0) vote_s[(gphase & 1) * 4 + (warp & 3)] = wany ? 1 : 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kGroup]);
+        if (!wwait(&bars[kGroup], gphase & 1)) return false;
+        const int base = (gphase & 1) * 4;
+        *any = vote_s[base] | vote_s[base + 1] | vote_s[base + 2] | vote_s[base + 3];
+        ++gphase;
+        return true;
+      };
+      SegIter it;
+      it.init(a.tile_start, U, lo, hi);
+      int32_t u, t0, nt, kslot;
+      bool whole;
+      uint32_t jglob = 0;
+      bool ok = true;
+      // PV #k (0-based, in this CTA's tile order) completes phase k/2 of p_free[k % 2].
+      // That barrier cannot run two phases ahead of this wait (its next phase needs
+      // P of tile k + 2, which this thread has not written), so the parity is exact.
+      auto wait_pv = [&](uint32_t k) -> bool { return wwait(&bars[kPFree0 + (k & 1)], (k >> 1) & 1); };
+      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+        const int b = u / a.n_held, rs = u % a.n_held;
+        const int64_t S = a.seq_lens[b];
+        const int grow = g * Rg + c;
+        const bool active = c < Rg && grow < a.R_total && S >= a.q_len;
+        int64_t nvis = 0;
+        if (active) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
+        float m_ref = -INFINITY, l = 0.f;
+        for (int jj = 0; jj < nt; ++jj, ++jglob) {
+          const int sb = jglob & 1;
+          if (!wwait(&bars[kSFull0 + sb], (jglob >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[64];
+          tmem_ld32(tmem + lane_base + 4 * Rg + kTile * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(tmem + lane_base + 4 * Rg + kTile * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
+          const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
+          const int64_t lim = nvis - rho0;  // columns k < lim are visible to this row
+          float mt = -INFINITY;
 #pragma unroll
-    for (int sh = 8; sh > 0; sh >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, sh));
-    const float m_new = fmaxf(m, tmax);
-    float p[2] = {0.f, 0.f};
-    float alpha = 1.f;
-    if (m_new != -INFINITY) {
-      alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
-      p[0] = exp2f(s[0] - m_new);
-      p[1] = exp2f(s[1] - m_new);
-    }
-    float psum = p[0] + p[1];
+          for (int k = 0; k < 64; ++k) {
+            const float xk = (k < lim) ? __uint_as_float(sr[k]) * a.scale_log2 : -INFINITY;
+            sr[k] = __float_as_uint(xk);
+            mt = fmaxf(mt, xk);
+          }
+          bool need = false;
+          float alpha = 1.f;
+          if (m_ref == -INFINITY) {
+            m_ref = mt;  // nothing accumulated yet for this row
+          } else if (mt > m_ref + kRescaleThreshold) {
+            need = true;
+            alpha = exp2f(m_ref - mt);
+            m_ref = mt;
+          }
+          alpha_s[(gphase & 1) * 128 + c] = alpha;
+          const uint32_t abuf = (gphase & 1) * 128;
+          bool any = false;
+          if (!group_sync(need, &any)) { ok = false; break; }
+          const int pb = jglob & 1;
+          if (!wwait(&bars[kPFree0 + pb], ((jglob >> 1) & 1) ^ 1)) { ok = false; break; }
+          if (any) {
+            // O^T columns of the rows whose maximum moved are scaled by alpha
+            if (!wait_pv(jglob - 1)) { ok = false; break; }
+            tc_fence_after();
+            for (int t = 0; t < 4; ++t) {
+              for (int c0 = 0; c0 < Rg; c0 += 16) {
+                uint32_t r[16];
+                const uint32_t addr = tmem + lane_base + t * Rg + c0;
+                tmem_ld16(addr, r);
+                tmem_ld_wait();
 #pragma unroll
-    for (int sh = 8; sh > 0; sh >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, sh);
-    l = l * alpha + psum;
-    m = m_new;
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[abuf + c0 + i]);
+                tmem_st16(addr, r);
+              }
+            }
+            tmem_st_wait();
+            l *= alpha;
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          float psum = 0.f;
+          uint32_t pk[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] *= alpha;
-    const int grp = (tid & 31) & 16;  // lane offset of this row's 16-lane group
-    for (int tok = 0; tok < kTile; ++tok) {
-      const float pt = __shfl_sync(0xffffffffu, p[tok >> 4], grp + (tok & 15));
-      const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(kv_s + tok * kKvPitch);
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = exp2f(__uint_as_float(sr[2 * k]) - m_use);
+            const float p1 = exp2f(__uint_as_float(sr[2 * k + 1]) - m_use);
+            psum += p0 + p1;
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          l += psum;
+          if (c < Rg) {
+            // row c of the K-major, 128B-swizzled P tile: 8 x 16-byte pieces
+            unsigned char* row = p_s + pb * Rg * 128 + (c >> 3) * 1024 + (c & 7) * 128;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float2 vf = __bfloat1622float2(vr[j + 16 * k]);
-        acc[2 * k] = fmaf(pt, vf.x, acc[2 * k]);
-        acc[2 * k + 1] = fmaf(pt, vf.y, acc[2 * k + 1]);
+            for (int q = 0; q < 8; ++q) {
+              uint4 w4 = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              *reinterpret_cast<uint4*>(row + ((q ^ (c & 7)) << 4)) = w4;
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kPFull0 + pb]);
+        }
+        if (!ok) break;
+        // ---------------- epilogue: O^T (dims x rows) / l -> o, lse
+        if (!wait_pv(jglob - 1)) { ok = false; break; }
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const uint32_t ibuf = (gphase & 1) * 128;
+        inv_s[ibuf + c] = inv;
+        const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+        bool dummy;
+        if (!group_sync(false, &dummy)) { ok = false; break; }
+        const int R_here = min(Rg, a.R_total - g * Rg);
+        const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total + g * Rg;
+        const int64_t piece = (int64_t)(2 * v + kslot) * a.R_total + g * Rg;
+        for (int t = 0; t < 4; ++t) {
+          for (int c0 = 0; c0 < Rg; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem + lane_base + t * Rg + c0, r);
+            tmem_ld_wait();
+            const int dim = t * 128 + c;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int row = c0 + i;
+              if (row < R_here) {
+                const float val = __uint_as_float(r[i]) * inv_s[ibuf + row];
+                if (whole) {
+                  if (a.o_bf16)
+                    static_cast<__nv_bfloat16*>(a.o_part)[(out_row0 + row) * kDv + dim] = __float2bfloat16_rn(val);
+                  else
+                    static_cast<float*>(a.o_part)[(out_row0 + row) * kDv + dim] = val;
+                } else {
+                  a.piece_o[(piece + row) * kDv + dim] = val;
+                }
+              }
+            }
+          }
+        }
+        if (c < R_here) {
+          if (whole)
+            a.lse_part[out_row0 + c] = a.base2 ? lse2 : lse2 * kLn2;
+          else
+            a.piece_lse[piece + c] = lse2;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kOFree]);
       }
     }
   }
 
-  const int row = row0 + i;
-  if (row >= R) return;
-  const int64_t out_row = ((int64_t)rs * a.B + b) * R + row;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  if (a.o_bf16) {
-    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) o[j + 16 * k] = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
-  } else {
-    float2* o = reinterpret_cast<float2*>(static_cast<float*>(a.o_part) + out_row * kDv);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) o[j + 16 * k] = make_float2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+  if (*abort_s && tid == 0) flag(a.status, DCP_STATUS_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------- fixup
+// Writes empty units (o = 0, lse = -inf) and merges the pieces of units cut by
+// range boundaries.  One block per unit.
+__global__ void __launch_bounds__(256) fixup_kernel(TcArgs a) {
+  const int32_t U = a.B * a.n_held;
+  const int32_t u = blockIdx.x;
+  if (u >= U) return;
+  const int b = u / a.n_held, rs = u % a.n_held;
+  const int64_t s = a.tile_start[u], e = a.tile_start[u + 1];
+  const int64_t T = a.tile_start[U];
+  const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total;
+  const int64_t nelem = (int64_t)a.R_total * kDv;
+  if (s == e) {
+    for (int64_t i = threadIdx.x; i < nelem; i += blockDim.x) {
+      if (a.o_bf16) static_cast<__nv_bfloat16*>(a.o_part)[out_row0 * kDv + i] = __float2bfloat16_rn(0.f);
+      else static_cast<float*>(a.o_part)[out_row0 * kDv + i] = 0.f;
+    }
+    for (int i = threadIdx.x; i < a.R_total; i += blockDim.x) a.lse_part[out_row0 + i] = -INFINITY;
+    return;
   }
-  if (j == 0) {
-    float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
-    a.lse_part[out_row] = a.base2 ? lse2 : lse2 * kLn2;
+  const int V = a.V;
+  auto part_of = [&](int64_t x) {  // range containing tile x
+    int vv = (int)((x * V) / T);
+    while (vv + 1 < V && range_lo(T, vv + 1, V) <= x) ++vv;
+    while (vv > 0 && range_lo(T, vv, V) > x) --vv;
+    return vv;
+  };
+  const int v0 = part_of(s), v1 = part_of(e - 1);
+  if (v0 == v1) return;  // written whole by the main kernel
+  // each thread handles (row, 4 dims) items
+  for (int64_t item = threadIdx.x; item < (int64_t)a.R_total * (kDv / 4); item += blockDim.x) {
+    const int row = (int)(item / (kDv / 4));
+    const int d4 = (int)(item % (kDv / 4)) * 4;
+    float m = -INFINITY;
+    for (int vv = v0; vv <= v1; ++vv) {
+      if (range_lo(T, vv, V) == range_lo(T, vv + 1, V)) continue;  // empty range: no piece
+      const int k = range_lo(T, vv, V) >= s ? 0 : 1;
+      m = fmaxf(m, a.piece_lse[(int64_t)(2 * vv + k) * a.R_total + row]);
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int vv = v0; vv <= v1; ++vv) {
+        if (range_lo(T, vv, V) == range_lo(T, vv + 1, V)) continue;
+        const int k = range_lo(T, vv, V) >= s ? 0 : 1;
+        const int64_t pr = (int64_t)(2 * vv + k) * a.R_total + row;
+        const float lv = a.piece_lse[pr];
+        if (lv == -INFINITY) continue;
+        const float w = exp2f(lv - m);
+        wsum += w;
+        const float4 o4 = *reinterpret_cast<const float4*>(a.piece_o + pr * kDv + d4);
+        acc[0] = fmaf(w, o4.x, acc[0]);
+        acc[1] = fmaf(w, o4.y, acc[1]);
+        acc[2] = fmaf(w, o4.z, acc[2]);
+        acc[3] = fmaf(w, o4.w, acc[3]);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t o_idx = (out_row0 + row) * kDv + d4;
+    for (int i = 0; i < 4; ++i) {
+      if (a.o_bf16) static_cast<__nv_bfloat16*>(a.o_part)[o_idx + i] = __float2bfloat16_rn(acc[i] * inv);
+      else static_cast<float*>(a.o_part)[o_idx + i] = acc[i] * inv;
+    }
+    if (d4 == 0) {
+      const float lse2 = wsum > 0.f ? m + log2f(wsum) : -INFINITY;
+      a.lse_part[out_row0 + row] = a.base2 ? lse2 : lse2 * kLn2;
+    }
   }
 }
 
-constexpr size_t kSmemBytes = kRowsPerCta * kDk * sizeof(float) + kTile * kKvPitch * sizeof(__nv_bfloat16);
+// ---------------------------------------------------------------------------- host side
+struct Plan {
+  int Rg, ngroups, V, nslot, box_rows;
+  size_t smem;
+  size_t ws_start_bytes, ws_piece_o_bytes, ws_piece_lse_bytes, ws_total;
+};
+
+int sm_count_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, Plan* p) {
+  const int R_total = q_len * H;
+  p->ngroups = (R_total + kMaxGroupRows - 1) / kMaxGroupRows;
+  const int per = (R_total + p->ngroups - 1) / p->ngroups;
+  p->Rg = ((per + 15) / 16) * 16;
+  const int sms = sm_count_current();
+  if (sms <= 0) return false;
+  p->V = sms / p->ngroups;
+  if (p->V < 1) p->V = 1;
+  const SmemLayout base = smem_layout(p->Rg, 0);
+  const size_t budget = 232448 - 1024;  // 227 KB minus alignment slack
+  int nslot = (int)((budget - base.total) / kChunkBytes);
+  nslot &= ~1;
+  if (nslot > kMaxSlots) nslot = kMaxSlots;
+  p->nslot = nslot;
+  p->smem = smem_layout(p->Rg, nslot).total + 1024;
+  const int P = layout->page_size;
+  p->box_rows = P >= kTile ? kTile : P;
+  const int64_t U = (int64_t)B * n_held;
+  p->ws_start_bytes = align256((size_t)(U + 1) * 4);
+  p->ws_piece_o_bytes = align256((size_t)2 * p->V * R_total * kDv * 4);
+  p->ws_piece_lse_bytes = align256((size_t)2 * p->V * R_total * 4);
+  p->ws_total = p->ws_start_bytes + p->ws_piece_o_bytes + p->ws_piece_lse_bytes;
+  return nslot >= 10;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [rows, 576] row-major, 128-byte swizzled boxes of [box_rows, 64]
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kChunkDims, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool page_size_ok(int P) { return P >= 8 && P % 8 == 0 && (P % kTile == 0 || kTile % P == 0); }
 
 }  // namespace
 
 extern "C" size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int32_t shard_begin,
                                                 int32_t shard_end, int32_t B, int32_t q_len, int32_t H) {
   if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end ||
-      B < 1 || q_len < 1 || H < 1)
+      B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > 1024)
     return 0;
-  return 0;
+  Plan p;
+  if (!make_plan(layout, shard_end - shard_begin, B, q_len, H, &p)) return 0;
+  return p.ws_total;
 }
 
 extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
@@ -208,34 +764,50 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(arena) |
        reinterpret_cast<uintptr_t>(o_part)) & 15)
     return DCP_ERR_INVALID;
-  const size_t need = dcp_mla_decode_workspace_size(layout, shard_begin, shard_end, B, q_len, H);
-  if (workspace_bytes < need || (need > 0 && !workspace)) return DCP_ERR_WORKSPACE;
+  if (!page_size_ok(layout->page_size)) return DCP_ERR_UNSUPPORTED;
+  const int n_held = shard_end - shard_begin;
+  const int64_t pool_rows = pool_pages * layout->page_size;
+  if ((int64_t)n_held * pool_rows >= INT32_MAX || (int64_t)B * q_len * H >= INT32_MAX ||
+      (int64_t)B * n_held >= INT32_MAX / 2)
+    return DCP_ERR_UNSUPPORTED;
+  Plan p;
+  if (!make_plan(layout, n_held, B, q_len, H, &p)) return DCP_ERR_CUDA;
+  if (!workspace || workspace_bytes < p.ws_total) return DCP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return DCP_ERR_INVALID;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(partial_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
+  CUtensorMap tq, tkv;
+  if (!make_tmap(&tq, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg)) return DCP_ERR_CUDA;
+  if (!make_tmap(&tkv, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
+
+  static size_t smem_set = 0;
+  if (smem_set < p.smem) {
+    if (cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
+        cudaSuccess)
       return DCP_ERR_CUDA;
-    attr_set = true;
+    smem_set = p.smem;
   }
-  PartialArgs a;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  TcArgs a;
   a.L = to_layout(layout);
   a.shard_begin = shard_begin;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.B = B; a.q_len = q_len; a.H = H;
-  a.arena = static_cast<const __nv_bfloat16*>(arena);
-  a.pool_pages = pool_pages;
-  a.pool_rows = pool_pages * layout->page_size;
+  a.n_held = n_held;
+  a.B = B; a.q_len = q_len; a.H = H; a.R_total = q_len * H;
+  a.Rg = p.Rg; a.ngroups = p.ngroups; a.V = p.V; a.nslot = p.nslot; a.box_rows = p.box_rows;
+  a.pool_rows = pool_rows; a.pool_pages = pool_pages;
   a.bt = block_table; a.bt_stride = bt_stride; a.max_pages = max_pages;
   a.seq_lens = seq_lens;
   a.scale_log2 = scale * kLog2e;
   a.base2 = lse_base == DCP_LSE_BASE_2;
   a.o_part = o_part; a.o_bf16 = o_part_dtype == DCP_BF16;
   a.lse_part = lse_part;
+  a.tile_start = reinterpret_cast<const int32_t*>(ws);
+  a.piece_o = reinterpret_cast<float*>(ws + p.ws_start_bytes);
+  a.piece_lse = reinterpret_cast<float*>(ws + p.ws_start_bytes + p.ws_piece_o_bytes);
   a.status = status;
-  const int R = q_len * H;
-  dim3 grid((R + kRowsPerCta - 1) / kRowsPerCta, shard_end - shard_begin, B);
-  if (B > 65535) return DCP_ERR_UNSUPPORTED;
-  partial_simt_kernel<<<grid, 256, kSmemBytes, as_stream(stream)>>>(a);
-  return launch_status();
+  cudaStream_t st = as_stream(stream);
+  const int32_t U = B * n_held;
+  plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
+  partial_tc_kernel<<<p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, a);
+  fixup_kernel<<<U, 256, 0, st>>>(a);
+  return launch_status(3);
 }

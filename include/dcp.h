@@ -72,7 +72,8 @@ enum {
   DCP_STATUS_BAD_PAGE_INDEX = 2,  /* local row / P >= max_pages */
   DCP_STATUS_BAD_PAGE_ID = 4,     /* block-table entry outside [0, pool_pages) */
   DCP_STATUS_BAD_REQUEST = 8,     /* request index outside [0, B) */
-  DCP_STATUS_BAD_LENGTH = 16      /* seq_len < q_len */
+  DCP_STATUS_BAD_LENGTH = 16,     /* seq_len < q_len */
+  DCP_STATUS_TIMEOUT = 32         /* a kernel pipeline wait gave up (the call's outputs are invalid) */
 };
 
 enum { DCP_LSE_BASE_E = 0, DCP_LSE_BASE_2 = 1 };

@@ -82,6 +82,47 @@ def test_needle_small(name):
     assert np.max(np.abs(avg - o[b, 0, h])) > 0.1
 
 
+@pytest.mark.parametrize("H,N", [(96, 8), (128, 8), (16, 4)])
+def test_running_max_jumps(H, N):
+    """Rows whose running maximum jumps several times inside one shard's stream.
+
+    Three planted rows (query copies scaled 0.5, 1.0, 1.5: scores ~20, 40, 60)
+    sit late in the sequence, so the kernel must rescale accumulated outputs
+    in the middle of a work range, with many tiles per CTA.
+    """
+    import context_sharded_mla_gb300 as dcp
+    from context_sharded_mla_gb300.step import ShardedMlaDecoder
+    S_total = 40000 + 33
+    cfg = workloads.config("k3", B=2, H=H, N=N, S=S_total)
+    S = workloads.lengths(cfg)
+    bt, pool_pages = workloads.block_table(cfg, S)
+    dev = "cuda"
+    lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
+    dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, 1,
+                            max_append=int(S.max()))
+    q = workloads.gen_q(cfg)
+    btd = bt.to(dev)
+    kvs = []
+    for b in range(cfg.B):
+        kv = workloads.gen_kv(cfg, b, int(S[b]))
+        for f, p in zip((0.5, 1.0, 1.5), (S_total // 2 + 7, 3 * S_total // 4 + 1, S_total - 100)):
+            kv[p] = (q[b, 0, b % H].float() * f).to(torch.bfloat16)
+        kvs.append(kv)
+        n = int(S[b])
+        dec.append(kv.to(dev), torch.arange(n, device=dev), torch.full((n,), b, dtype=torch.int32, device=dev), btd)
+    o, lse = dec.decode(q.to(dev), btd, S.to(dev))
+    torch.cuda.synchronize()
+    assert dec.status_bits() == 0
+    for b in range(cfg.B):
+        ro, rl, rop, rlp = attention.sharded_attention(to_f64(q[b]), to_f64(kvs[b]), int(S[b]), cfg.N, cfg.I,
+                                                       workloads.SCALE, 2)
+        assert_close_o(to_f64(o[b]), ro, "jump o")
+        assert_close_lse(to_f64(lse[b]), rl, "jump lse")
+        for r in range(cfg.N):
+            assert_close_o(to_f64(dec.o_part[r, b]), rop[r], f"jump o_part r={r}")
+            assert_close_lse(to_f64(dec.lse_part[r, b]), rlp[r], f"jump lse_part r={r}")
+
+
 def test_bf16_partials():
     cfg = workloads.config("k3", **SMALL["k3"])
     st = GpuState(cfg, part_dtype=torch.bfloat16)
