@@ -10,26 +10,24 @@
 // rank and the global lengths).
 //
 // Design (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: query rows once per segment; KV tiles of 64 local
-//               rows x 64 dims ("chunks", 8 KB, 128-byte swizzle) into a ring.
+//   warp 0      TMA producer: the 64 rope dims of the query rows once per
+//               segment; KV tiles of 64 local rows x 64 dims ("chunks", 8 KB,
+//               128-byte swizzle) into a ring of ~24 chunk slots.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
-//   warps 2-5   softmax (one query row per thread) and epilogue.
-// Per KV tile j of 64 rows:
-//   S_j   = Q K_j^T            M=128 query rows (R_g valid), N=64 rows, K=576   (TMEM, fp32)
+//   warps 2-5   load the 512 c_K dims of the query rows into TMEM once per
+//               segment, then softmax (one query row per thread) and epilogue.
+// Query rows are processed in groups of at most 48 (one CTA per group), so that
+// TMEM (512 columns) holds O^T (4 x 48 columns), one S tile (64) and the query's
+// c_K part as the MMA A operand (256 columns: 512 bf16 per lane).  Per tile j:
+//   S_j   = Q K_j^T            M=128 rows (A: TMEM for dims 0-511, smem for the
+//                              64 rope dims), N=64 KV rows, K=576        -> TMEM fp32
 //   P_j   = exp2(S_j*scale*log2e - m)      online softmax with lazy rescaling
-//   O^T  += V_j^T P_j^T        M=128 value dims (x4 tiles), N=R_g rows, K=64  (TMEM, fp32)
-// O is kept transposed (dims on TMEM lanes, query rows on columns) so that 4*R_g
-// columns of fp32 accumulator plus two 64-column S buffers fit in 512 columns.
-// The tile's V chunks are fetched a second time for the PV product (from L2)
-// because the 576-d K pass and the query block leave no room to keep a tile.
+//   O^T  += V_j^T P_j^T        M=128 value dims (x4), N=rows, K=64 KV rows -> TMEM fp32
+// The tile's chunks 0-7 stay in the ring from the QK product to the PV product
+// (V = the first 512 dims of the same rows), so every KV byte crosses HBM and
+// shared memory once.  O is kept transposed (dims on TMEM lanes) so the
+// accumulator needs only 4 columns per query row.
 //
-// Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
-// concatenation of all units' tiles is cut into V equal ranges, one per CTA (or
-// per group of CTAs when the query rows need several row groups).  A unit that
-// lies inside one range is written directly; a unit cut by range boundaries
-// leaves normalised pieces (o, lse in base 2) in the workspace which a second
-// kernel merges with the same LSE rule.  A third tiny kernel (run first) writes
-// the tile prefix sums.
 #include <cudaTypedefs.h>
 
 #include "dcp_internal.cuh"
@@ -44,14 +42,14 @@ constexpr int kTile = 64;          // KV rows per tile
 constexpr int kChunkDims = 64;     // dims per chunk (one 128-byte swizzle row)
 constexpr int kNumChunks = 9;      // 576 / 64
 constexpr int kChunkBytes = kTile * 128;
-constexpr int kKSlots = 10;        // ring uses per K pass (9 chunks + 1 unused, keeps V pairs aligned)
-constexpr int kVSlots = 8;         // ring uses per V pass (chunks 0..7)
-constexpr int kMaxSlots = 24;
+constexpr int kKSlots = 10;        // ring uses per tile (9 chunks + 1 unused: V chunk pairs start on even slots)
+constexpr int kMaxSlots = 26;
+constexpr int kQTmemCol = 256;     // TMEM columns [256, 512): query dims 0-511 as bf16 pairs
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
-constexpr int kMaxGroupRows = 96;
+constexpr int kMaxGroupRows = 48;
 
 struct TcArgs {
   Layout L;
@@ -59,6 +57,7 @@ struct TcArgs {
   int32_t B, q_len, H, R_total;  // R_total = q_len * H
   int32_t Rg, ngroups, V;        // rows per group, groups, stream-K ranges
   int32_t nslot;
+  int32_t nsbuf;                 // S tiles in TMEM (1 or 2)
   int32_t box_rows;              // KV TMA box height = min(P, 64)
   int64_t pool_rows, pool_pages;
   const int32_t* bt;
@@ -69,6 +68,7 @@ struct TcArgs {
   void* o_part;
   int32_t o_bf16;
   float* lse_part;
+  const __nv_bfloat16* q;     // [B * R_total][576]
   const int32_t* tile_start;  // [U + 1]
   float* piece_o;             // [2V][R_total][512]
   float* piece_lse;           // [2V][R_total]
@@ -81,8 +81,8 @@ struct SmemLayout {
 
 __host__ __device__ inline SmemLayout smem_layout(int Rg, int nslot) {
   SmemLayout s;
-  s.q = 0;
-  s.ring = kNumChunks * Rg * 128;
+  s.q = 0;                          // rope dims of the query rows: [Rg][64] bf16
+  s.ring = Rg * 128;
   s.p = s.ring + nslot * kChunkBytes;
   s.alpha = s.p + 2 * Rg * 128;
   s.inv = s.alpha + 2 * 128 * 4;
@@ -190,6 +190,14 @@ struct SegIter {
 
 __device__ inline int64_t range_lo(int64_t T, int v, int V) { return (T * v) / V; }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22,
+// 2^-inf = +0); the result is rounded to bf16 for the PV product anyway.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------- main kernel
 __global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
@@ -198,11 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemLayout sl = smem_layout(a.Rg, a.nslot);
-  unsigned char* q_s = smem + sl.q;
+  unsigned char* qr_s = smem + sl.q;
   unsigned char* ring = smem + sl.ring;
   unsigned char* p_s = smem + sl.p;
-  float* alpha_s = reinterpret_cast<float*>(smem + sl.alpha);  // [2][128]
-  float* inv_s = reinterpret_cast<float*>(smem + sl.inv);      // [2][128]
+  float* alpha_s = reinterpret_cast<float*>(smem + sl.alpha);              // [2][128]
+  float* inv_s = reinterpret_cast<float*>(smem + sl.inv);                  // [2][128]
   volatile int* vote_s = reinterpret_cast<volatile int*>(smem + sl.vote);  // [2][4]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
   uint64_t* full = bars + kNumFixedBars;
@@ -217,11 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = blockIdx.x % a.ngroups;
   const int Rg = a.Rg;
   const int nslot = a.nslot;
+  const int nsbuf = a.nsbuf;
   const int32_t U = a.B * a.n_held;
 
   if (tid == 0) {
     *abort_s = 0;
     for (int i = 0; i < kNumFixedBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[kQFull], 5);   // producer (rope TMA bytes) + 4 warps storing Q into TMEM
     mbar_init(&bars[kSFree0], 4);
     mbar_init(&bars[kSFree1], 4);
     mbar_init(&bars[kPFull0], 4);
@@ -234,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_barrier_init();
   }
-  // stale ring rows past a request's last page are read (with zero weight):
-  // start from finite zeros
+  // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nslot * kChunkBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
@@ -260,44 +269,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(a.tile_start, U, lo, hi);
       int32_t u, t0, nt, kslot;
       bool whole;
-      uint32_t use = 0;  // ring uses so far
+      uint32_t use = 0;  // ring uses so far (kKSlots per tile)
       int seg = 0;
       bool ok = true;
-      auto load_pass = [&](int b, int rs, int64_t nvis, int32_t tile, bool kpass) -> bool {
+      // KV boxes of one tile: page ids are fetched one tile ahead (raw loads whose
+      // results are consumed a tile later), so block-table latency never sits
+      // between two TMA issues.
+      struct Boxes {
+        int32_t y[8];
+        uint32_t bytes;
+      };
+      const int nbox = kTile / a.box_rows;
+      auto fetch_pages = [&](int b, int64_t nvis, int32_t tile, int32_t (&pg)[8]) {
         const int64_t rho0 = (int64_t)tile * kTile;
-        const int nchunks = kpass ? kNumChunks : kVSlots;
-        const int nuses = kpass ? kKSlots : kVSlots;
-        for (int k = 0; k < nuses; ++k) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          pg[q] = -2;  // not needed
+          const int64_t rho = rho0 + (int64_t)q * a.box_rows;
+          if (q < nbox && rho < nvis) {
+            const int64_t pidx = rho / a.L.P;
+            pg[q] = pidx < a.max_pages ? __ldg(a.bt + (int64_t)b * a.bt_stride + pidx) : -1;
+          }
+        }
+      };
+      auto make_boxes = [&](int rs, int32_t tile, const int32_t (&pg)[8], Boxes& bx) {
+        const int64_t rho0 = (int64_t)tile * kTile;
+        bx.bytes = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          bx.y[q] = -1;
+          if (pg[q] == -2) continue;
+          if (pg[q] < 0 || pg[q] >= a.pool_pages) {
+            flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+            continue;
+          }
+          const int64_t rho = rho0 + (int64_t)q * a.box_rows;
+          bx.y[q] = (int32_t)((int64_t)rs * a.pool_rows + (int64_t)pg[q] * a.L.P + rho % a.L.P);
+          bx.bytes += a.box_rows * 128;
+        }
+      };
+      auto load_tile = [&](const Boxes& bx) -> bool {
+        for (int k = 0; k < kKSlots; ++k) {
           const uint32_t slot = use % nslot;
           const uint32_t round = use / nslot;
           if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_s)) return false;
-          unsigned char* dst = ring + slot * kChunkBytes;
-          if (k >= nchunks) {
+          if (k >= kNumChunks) {
             mbar_arrive(&full[slot]);
           } else {
-            // boxes of box_rows rows covering local rows [rho0, rho0 + 64)
-            int nbox = kTile / a.box_rows;
-            uint32_t bytes = 0;
-            int64_t ys[kTile / 8];
-            int nvalid = 0;
-            for (int q = 0; q < nbox; ++q) {
-              const int64_t rho = rho0 + (int64_t)q * a.box_rows;
-              ys[q] = -1;
-              if (rho >= nvis) continue;
-              const int64_t pidx = rho / a.L.P;
-              int64_t page = pidx < a.max_pages ? (int64_t)a.bt[(int64_t)b * a.bt_stride + pidx] : -1;
-              if (page < 0 || page >= a.pool_pages) {
-                flag(a.status, DCP_STATUS_BAD_PAGE_ID);
-                continue;
-              }
-              ys[q] = (int64_t)rs * a.pool_rows + page * a.L.P + rho % a.L.P;
-              bytes += a.box_rows * 128;
-              ++nvalid;
-            }
-            mbar_arrive_expect_tx(&full[slot], bytes);
-            for (int q = 0; q < nbox; ++q)
-              if (ys[q] >= 0)
-                tma_load_2d(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, (int32_t)ys[q]);
+            unsigned char* dst = ring + slot * kChunkBytes;
+            mbar_arrive_expect_tx(&full[slot], bx.bytes);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (bx.y[q] >= 0) tma_load_2d(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, bx.y[q]);
           }
           ++use;
         }
@@ -307,17 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = u / a.n_held, rs = u % a.n_held;
         bool bad = false;
         const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
+        int32_t pg_next[8];
+        fetch_pages(b, nvis, t0, pg_next);
         if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kQFull], kNumChunks * Rg * 128);
-        const int32_t qrow = b * a.R_total + g * Rg;
-        for (int k = 0; k < kNumChunks; ++k)
-          tma_load_2d(q_s + k * Rg * 128, &tmap_q, &bars[kQFull], k * kChunkDims, qrow);
+        mbar_arrive_expect_tx(&bars[kQFull], Rg * 128);
+        tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 8 * kChunkDims, b * a.R_total + g * Rg);
         ++seg;
+        Boxes cur;
+        make_boxes(rs, t0, pg_next, cur);
         for (int jj = 0; jj < nt && ok; ++jj) {
-          ok = load_pass(b, rs, nvis, t0 + jj, true);
-          if (ok && jj >= 1) ok = load_pass(b, rs, nvis, t0 + jj - 1, false);
+          if (jj + 1 < nt) fetch_pages(b, nvis, t0 + jj + 1, pg_next);
+          ok = load_tile(cur);
+          if (jj + 1 < nt) make_boxes(rs, t0 + jj + 1, pg_next, cur);
         }
-        if (ok) ok = load_pass(b, rs, nvis, t0 + nt - 1, false);
       }
       if (!ok) {
         // drain: wait (bounded, ignoring the abort flag) for copies already issued
@@ -328,103 +353,150 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (!mbar_try_wait(&full[slot], (uu / nslot) & 1) && globaltimer() - t0n < kWaitLimitNs) {
           }
         }
-        const uint64_t t0n = globaltimer();
-        while (!mbar_try_wait(&bars[kQFull], (seg - 1) & 1) && seg > 0 && globaltimer() - t0n < kWaitLimitNs) {
-        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Event-driven single thread: QK chunks are issued as their data lands and
+    // each PV product as soon as its P tile is ready, so a PV never waits behind
+    // the next tile's loads (the PV releases the ring slots those loads need).
     if (lane == 0 && lo < hi) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, Rg, 1, 0);
-      const uint32_t q_addr = smem_u32(q_s);
-      const uint32_t ring_addr = smem_u32(ring);
-      const uint32_t p_addr = smem_u32(p_s);
-      SegIter it;
-      it.init(a.tile_start, U, lo, hi);
-      int32_t u, t0, nt, kslot;
-      bool whole;
-      uint32_t use = 0;
-      uint32_t jglob = 0;  // tiles started by this CTA
-      int seg = 0;
-      bool ok = true;
-      auto qk = [&](uint32_t j) -> bool {
-        const int sb = j & 1;
-        if (!mbar_wait(&bars[kSFree0 + sb], ((j >> 1) & 1) ^ 1, abort_s)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + 4 * Rg + kTile * sb;
-        for (int k = 0; k < kKSlots; ++k) {
-          const uint32_t slot = use % nslot, round = use / nslot;
-          if (!mbar_wait(&full[slot], round & 1, abort_s)) return false;
-          if (k < kNumChunks) {
-            tc_fence_after();
-            const uint32_t kaddr = ring_addr + slot * kChunkBytes;
-            const uint32_t qaddr = q_addr + k * Rg * 128;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, sw128_desc(qaddr + kk * 32, 16, 1024), sw128_desc(kaddr + kk * 32, 16, 1024), idesc_qk,
-                          (k | kk) != 0);
-            mma_commit(&empty[slot]);
-          } else {
-            mbar_arrive(&empty[slot]);
-          }
-          ++use;
-        }
-        mma_commit(&bars[kSFull0 + sb]);
-        return true;
-      };
-      auto pv = [&](uint32_t j, bool first) -> bool {
-        const int pb = j & 1;
-        if (!mbar_wait(&bars[kPFull0 + pb], (j >> 1) & 1, abort_s)) return false;
-        if (first && seg >= 2) {
-          if (!mbar_wait(&bars[kOFree], (seg - 2) & 1, abort_s)) return false;
-        }
-        tc_fence_after();
-        const uint32_t pbase = p_addr + pb * Rg * 128;
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t slot = use % nslot, round = use / nslot;
-          const uint32_t slot2 = (use + 1) % nslot, round2 = (use + 1) / nslot;
-          if (!mbar_wait(&full[slot], round & 1, abort_s)) return false;
-          if (!mbar_wait(&full[slot2], round2 & 1, abort_s)) return false;
-          tc_fence_after();
-          const uint32_t vaddr = ring_addr + slot * kChunkBytes;
-          const uint32_t d = tmem + t * Rg;
+      // descriptor templates; a byte offset is added to the start-address field (>> 4)
+      const uint64_t kdesc0 = sw128_desc(smem_u32(ring), 16, 1024);
+      const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
+      const uint64_t qrdesc0 = sw128_desc(smem_u32(qr_s), 16, 1024);
+      const uint64_t pdesc0 = sw128_desc(smem_u32(p_s), 16, 1024);
+      auto issue_qk_chunk = [&](uint32_t j, int k, uint32_t slot) {
+        const uint32_t d = tmem + 4 * Rg + kTile * (j % nsbuf);
+        const uint64_t kd = kdesc0 + ((slot * kChunkBytes) >> 4);
+        if (k < 8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, sw128_desc(vaddr + kk * 2048, kChunkBytes, 1024), sw128_desc(pbase + kk * 32, 16, 1024),
-                        idesc_pv, !(first && kk == 0));
+            mma_bf16_ts(d, tmem + kQTmemCol + k * 32 + kk * 8, kd + kk * 2, idesc_qk, (k | kk) != 0);
+        } else if (k == 8) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + kk * 2, kd + kk * 2, idesc_qk, 1);
+          mma_commit(&empty[slot]);  // the rope chunk is not needed by the PV product
+        } else {
+          mbar_arrive(&empty[slot]);
+        }
+      };
+      auto issue_pv = [&](uint32_t j, bool first) {
+        const int pb = j & 1;
+        const uint64_t pd = pdesc0 + ((pb * Rg * 128) >> 4);
+        const uint32_t base = j * kKSlots;
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t slot = (base + 2 * t) % nslot;  // even: the pair (2t, 2t+1) is contiguous
+          const uint64_t vd = vdesc0 + ((slot * kChunkBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + t * Rg, vd + kk * (2048 >> 4), pd + kk * 2, idesc_pv, !(first && kk == 0));
           mma_commit(&empty[slot]);
-          mma_commit(&empty[slot2]);
-          use += 2;
+          mma_commit(&empty[slot + 1]);
         }
         mma_commit(&bars[kPFree0 + pb]);
-        return true;
       };
-      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
-        if (!mbar_wait(&bars[kQFull], seg & 1, abort_s)) { ok = false; break; }
-        ++seg;
-        const uint32_t jfirst = jglob;
-        for (int jj = 0; jj < nt && ok; ++jj) {
-          ok = qk(jglob);
-          if (ok && jj == nt - 1) mma_commit(&bars[kQEmpty]);
-          if (ok && jj >= 1) ok = pv(jglob - 1, jglob - 1 == jfirst);
-          ++jglob;
+      // QK cursor
+      SegIter itq;
+      itq.init(a.tile_start, U, lo, hi);
+      int32_t uq, t0q, ntq, ksq;
+      bool wq;
+      bool q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
+      int q_seg = 0, q_jj = 0, q_k = 0;
+      bool q_seg_ready = false, q_tile_ready = false;
+      uint32_t jq = 0;
+      // PV cursor
+      SegIter itp;
+      itp.init(a.tile_start, U, lo, hi);
+      int32_t up, t0p, ntp, ksp;
+      bool wp;
+      bool p_has = itp.next(&up, &t0p, &ntp, &wp, &ksp);
+      int p_seg = 0, p_jj = 0;
+      uint32_t jp = 0;
+      uint64_t idle_since = 0;
+      while (q_has || p_has) {
+        bool progress = false;
+        if (p_has && jp < jq) {
+          bool ready = mbar_try_wait(&bars[kPFull0 + (jp & 1)], (jp >> 1) & 1);
+          if (ready && p_jj == 0 && p_seg >= 1) ready = mbar_try_wait(&bars[kOFree], (p_seg - 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            issue_pv(jp, p_jj == 0);
+            ++jp;
+            if (++p_jj == ntp) {
+              ++p_seg;
+              p_jj = 0;
+              p_has = itp.next(&up, &t0p, &ntp, &wp, &ksp);
+            }
+            progress = true;
+          }
         }
-        if (ok) ok = pv(jglob - 1, jglob - 1 == jfirst);
+        if (q_has) {
+          if (!q_seg_ready && mbar_try_wait(&bars[kQFull], q_seg & 1)) {
+            q_seg_ready = true;
+            progress = true;
+          }
+          if (q_seg_ready && !q_tile_ready &&
+              mbar_try_wait(&bars[kSFree0 + (jq % nsbuf)], ((jq / nsbuf) & 1) ^ 1)) {
+            q_tile_ready = true;
+            progress = true;
+          }
+          if (q_tile_ready) {
+            while (q_k < kKSlots) {
+              const uint32_t use = jq * kKSlots + q_k;
+              const uint32_t slot = use % nslot;
+              if (!mbar_try_wait(&full[slot], (use / nslot) & 1)) break;
+              tc_fence_after();
+              issue_qk_chunk(jq, q_k, slot);
+              ++q_k;
+              progress = true;
+            }
+            if (q_k == kKSlots) {
+              mma_commit(&bars[kSFull0 + (jq % nsbuf)]);
+              if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
+              ++jq;
+              q_k = 0;
+              q_tile_ready = false;
+              if (++q_jj == ntq) {
+                ++q_seg;
+                q_jj = 0;
+                q_seg_ready = false;
+                q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
+              }
+            }
+          }
+        }
+        if (progress) {
+          idle_since = 0;
+        } else {
+          if (*abort_s) break;
+          const uint64_t now = globaltimer();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > kWaitLimitNs) {
+            *abort_s = 1;
+            break;
+          }
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue
+    // ------------------------------------------------------------------ Q load, softmax, epilogue
     // All waits here are warp-uniform (every lane waits, then __all_sync), and the
-    // four warps meet only through the bounded kGroup mbarrier, so a timeout
-    // anywhere drains every thread instead of stranding some at a barrier.
-    const int c = 32 * (warp & 3) + lane;        // TMEM lane: query row (S) / value dim (O^T)
+    // four warps meet only through bounded mbarriers, so a timeout anywhere
+    // drains every thread instead of stranding some at a barrier.
+    const int c = 32 * (warp & 3) + lane;        // TMEM lane: query row (S, Q) / value dim (O^T)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     if (lo < hi) {
+      // one lane polls the barrier (128 spinning lanes would crowd the producer's
+      // TMA and barrier traffic); the warp then synchronises on its result
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        const bool r = mbar_wait(bar, parity, abort_s);
-        return __all_sync(0xffffffffu, r);
+        int r = 1;
+        if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
+        r = __shfl_sync(0xffffffffu, r, 0);
+        return r != 0;
       };
       uint32_t gphase = 0;  // kGroup phases passed
       // every softmax warp arrives; returns the OR of the warps' flags
@@ -444,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t u, t0, nt, kslot;
       bool whole;
       uint32_t jglob = 0;
+      int seg = 0;
       bool ok = true;
       // PV #k (0-based, in this CTA's tile order) completes phase k/2 of p_free[k % 2].
       // That barrier cannot run two phases ahead of this wait (its next phase needs
@@ -456,10 +529,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool active = c < Rg && grow < a.R_total && S >= a.q_len;
         int64_t nvis = 0;
         if (active) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
+        // ---- query dims 0-511 of this row -> TMEM lane c, columns [256, 512)
+        if (!wwait(&bars[kQEmpty], (seg & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const bool has_row = c < Rg && grow < a.R_total;
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk);
+          for (int i = 0; i < 8; ++i) {
+            uint32_t r[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              uint4 w4 = has_row ? __ldg(src + 8 * i + k) : make_uint4(0, 0, 0, 0);
+              r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
+            }
+            tmem_st32(tmem + lane_base + kQTmemCol + 32 * i, r);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kQFull]);
+        ++seg;
         float m_ref = -INFINITY, l = 0.f;
         for (int jj = 0; jj < nt; ++jj, ++jglob) {
-          const int sb = jglob & 1;
-          if (!wwait(&bars[kSFull0 + sb], (jglob >> 1) & 1)) { ok = false; break; }
+          const int sb = jglob % nsbuf;
+          if (!wwait(&bars[kSFull0 + sb], (jglob / nsbuf) & 1)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[64];
           tmem_ld32(tmem + lane_base + 4 * Rg + kTile * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -470,13 +564,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
           const int64_t lim = nvis - rho0;  // columns k < lim are visible to this row
-          float mt = -INFINITY;
+          if (lim < kTile) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float xk = (k < lim) ? __uint_as_float(sr[k]) * a.scale_log2 : -INFINITY;
-            sr[k] = __float_as_uint(xk);
-            mt = fmaxf(mt, xk);
+            for (int k = 0; k < 64; ++k)
+              if (k >= lim) sr[k] = __float_as_uint(-INFINITY);
           }
+          float mraw = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 64; ++k) mraw = fmaxf(mraw, __uint_as_float(sr[k]));
+          const float mt = mraw * a.scale_log2;  // scale > 0: the max commutes with the scaling
           bool need = false;
           float alpha = 1.f;
           if (m_ref == -INFINITY) {
@@ -486,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             alpha = exp2f(m_ref - mt);
             m_ref = mt;
           }
-          alpha_s[(gphase & 1) * 128 + c] = alpha;
           const uint32_t abuf = (gphase & 1) * 128;
+          alpha_s[abuf + c] = alpha;
           bool any = false;
           if (!group_sync(need, &any)) { ok = false; break; }
           const int pb = jglob & 1;
@@ -511,12 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const float cs = a.scale_log2;
           float psum = 0.f;
           uint32_t pk[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float p0 = exp2f(__uint_as_float(sr[2 * k]) - m_use);
-            const float p1 = exp2f(__uint_as_float(sr[2 * k + 1]) - m_use);
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * k]), cs, -m_use));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * k + 1]), cs, -m_use));
             psum += p0 + p1;
             __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             pk[k] = *reinterpret_cast<uint32_t*>(&h);
@@ -664,7 +761,7 @@ __global__ void __launch_bounds__(256) fixup_kernel(TcArgs a) {
 
 // ---------------------------------------------------------------------------- host side
 struct Plan {
-  int Rg, ngroups, V, nslot, box_rows;
+  int Rg, ngroups, V, nslot, nsbuf, box_rows;
   size_t smem;
   size_t ws_start_bytes, ws_piece_o_bytes, ws_piece_lse_bytes, ws_total;
 };
@@ -693,6 +790,7 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   nslot &= ~1;
   if (nslot > kMaxSlots) nslot = kMaxSlots;
   p->nslot = nslot;
+  p->nsbuf = (4 * p->Rg + 2 * kTile <= kQTmemCol) ? 2 : 1;
   p->smem = smem_layout(p->Rg, nslot).total + 1024;
   const int P = layout->page_size;
   p->box_rows = P >= kTile ? kTile : P;
@@ -701,7 +799,7 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   p->ws_piece_o_bytes = align256((size_t)2 * p->V * R_total * kDv * 4);
   p->ws_piece_lse_bytes = align256((size_t)2 * p->V * R_total * 4);
   p->ws_total = p->ws_start_bytes + p->ws_piece_o_bytes + p->ws_piece_lse_bytes;
-  return nslot >= 10;
+  return nslot >= 2 * kKSlots;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -792,7 +890,8 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   a.shard_begin = shard_begin;
   a.n_held = n_held;
   a.B = B; a.q_len = q_len; a.H = H; a.R_total = q_len * H;
-  a.Rg = p.Rg; a.ngroups = p.ngroups; a.V = p.V; a.nslot = p.nslot; a.box_rows = p.box_rows;
+  a.Rg = p.Rg; a.ngroups = p.ngroups; a.V = p.V; a.nslot = p.nslot; a.nsbuf = p.nsbuf; a.box_rows = p.box_rows;
+  a.q = static_cast<const __nv_bfloat16*>(q);
   a.pool_rows = pool_rows; a.pool_pages = pool_pages;
   a.bt = block_table; a.bt_stride = bt_stride; a.max_pages = max_pages;
   a.seq_lens = seq_lens;
