@@ -9,25 +9,33 @@
 // "DCP x speculative decoding" (causal mask in global positions, from the shard
 // rank and the global lengths).
 //
-// Design (one persistent CTA per SM, 192 threads):
+// Design: persistent 2-CTA clusters (one CTA per SM, 192 threads each):
 //   warp 0      TMA producer: the 64 rope dims of the query rows once per
 //               segment; KV tiles of 64 local rows x 64 dims ("chunks", 8 KB,
-//               128-byte swizzle) into a ring of ~24 chunk slots.
+//               128-byte swizzle) into a ring of ~22 chunk slots.  Each chunk is
+//               fetched once and multicast into both CTAs of the cluster.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
 //   warps 2-5   load the 512 c_K dims of the query rows into TMEM once per
 //               segment, then softmax (one query row per thread) and epilogue.
-// Query rows are processed in groups of at most 48 (one CTA per group), so that
-// TMEM (512 columns) holds O^T (4 x 48 columns), one S tile (64) and the query's
-// c_K part as the MMA A operand (256 columns: 512 bf16 per lane).  Per tile j:
+// A cluster handles a group of at most 96 query rows.  Both CTAs compute the
+// same S and P; CTA r keeps value dims [256 r, 256 r + 256).  TMEM per CTA:
+// O^T (2 x 96 columns), one S tile (64) and the query's c_K part as the MMA A
+// operand (256 columns).  Per tile j:
 //   S_j   = Q K_j^T            M=128 rows (A: TMEM for dims 0-511, smem for the
 //                              64 rope dims), N=64 KV rows, K=576        -> TMEM fp32
 //   P_j   = exp2(S_j*scale*log2e - m)      online softmax with lazy rescaling
-//   O^T  += V_j^T P_j^T        M=128 value dims (x4), N=rows, K=64 KV rows -> TMEM fp32
-// The tile's chunks 0-7 stay in the ring from the QK product to the PV product
-// (V = the first 512 dims of the same rows), so every KV byte crosses HBM and
-// shared memory once.  O is kept transposed (dims on TMEM lanes) so the
-// accumulator needs only 4 columns per query row.
+//   O^T  += V_j^T P_j^T        M=128 value dims (x2), N=rows, K=64 KV rows -> TMEM fp32
+// The tile's chunks stay in the ring from the QK product to the PV product
+// (V = the first 512 dims of the same rows), so every KV byte crosses HBM once
+// and reaches each SM's shared memory once.  O is kept transposed (dims on
+// TMEM lanes) so the accumulator needs only 2 columns per query row per CTA.
 //
+// Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
+// concatenation of all units' tiles is cut into V equal ranges, one per cluster
+// (per row group).  A unit inside one range is written directly; a unit cut by
+// range boundaries leaves normalised pieces (o, lse in base 2) in the workspace
+// which a second kernel merges with the same LSE rule.  A tiny kernel run first
+// writes the tile prefix sums.
 #include <cudaTypedefs.h>
 
 #include "dcp_internal.cuh"
@@ -45,11 +53,12 @@ constexpr int kChunkBytes = kTile * 128;
 constexpr int kKSlots = 10;        // ring uses per tile (9 chunks + 1 unused: V chunk pairs start on even slots)
 constexpr int kMaxSlots = 26;
 constexpr int kQTmemCol = 256;     // TMEM columns [256, 512): query dims 0-511 as bf16 pairs
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;     // 7 warps: 2 producers, 1 MMA issuer, 4 softmax/epilogue
+constexpr int kProducerWarpB = 6;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
-constexpr int kMaxGroupRows = 48;
+constexpr int kMaxGroupRows = 96;
 
 struct TcArgs {
   Layout L;
@@ -199,7 +208,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------------------- main kernel
-__global__ void __launch_bounds__(kThreads, 1)
+// A 2-CTA cluster per work range.  Both CTAs compute the same S and P for the
+// group's rows; CTA `rank` accumulates value dims [256 rank, 256 rank + 256)
+// (value chunks 4 rank .. 4 rank + 3).  Every KV chunk is fetched once and
+// multicast into both CTAs' rings (rank 0 issues the even chunks, rank 1 the odd
+// ones); a slot is refilled only when both CTAs have released it.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
                       TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -221,12 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int v = blockIdx.x / a.ngroups;
-  const int g = blockIdx.x % a.ngroups;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int cid = blockIdx.x >> 1;  // cluster index
+  const int v = cid / a.ngroups;
+  const int g = cid % a.ngroups;
   const int Rg = a.Rg;
   const int nslot = a.nslot;
   const int nsbuf = a.nsbuf;
   const int32_t U = a.B * a.n_held;
+  constexpr uint16_t kBoth = 0x3;
 
   if (tid == 0) {
     *abort_s = 0;
@@ -239,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kOFree], 4);
     mbar_init(&bars[kGroup], 4);
     for (int i = 0; i < nslot; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], 1);    // own producer's expect_tx; bytes from both CTAs' copies
+      mbar_init(&empty[i], 2);   // released by both CTAs' MMA issuers
     }
     fence_barrier_init();
   }
@@ -253,15 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before any multicast copy or remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
   const int64_t T = a.tile_start[U];
   const int64_t lo = range_lo(T, v, a.V), hi = range_lo(T, v + 1, a.V);
+  const uint32_t ntiles_cta = (uint32_t)(hi - lo);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 0 || warp == kProducerWarpB) {
+    // ------------------------------------------------------------------ producers
+    // Two producer threads split each tile's ring uses by parity (producer pp
+    // handles chunks k = pp, pp + 2, ...), halving the per-use barrier/TMA
+    // latency chain; slot parity equals use parity, so each owns half the slots.
+    const int pp = warp == 0 ? 0 : 1;
     if (lane == 0 && lo < hi) {
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_kv);
@@ -269,17 +292,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(a.tile_start, U, lo, hi);
       int32_t u, t0, nt, kslot;
       bool whole;
-      uint32_t use = 0;  // ring uses so far (kKSlots per tile)
+      uint32_t tile_base = 0;  // first ring use of the current tile (kKSlots per tile)
       int seg = 0;
       bool ok = true;
-      // KV boxes of one tile: page ids are fetched one tile ahead (raw loads whose
-      // results are consumed a tile later), so block-table latency never sits
-      // between two TMA issues.
+      // page ids are fetched one tile ahead (raw loads consumed a tile later)
       struct Boxes {
         int32_t y[8];
         uint32_t bytes;
       };
       const int nbox = kTile / a.box_rows;
+      auto box_y = [](const Boxes& bx, int q) -> int32_t {  // register-resident select (no local memory)
+        int32_t y = bx.y[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+          if (q == i) y = bx.y[i];
+        return y;
+      };
       auto fetch_pages = [&](int b, int64_t nvis, int32_t tile, int32_t (&pg)[8]) {
         const int64_t rho0 = (int64_t)tile * kTile;
 #pragma unroll
@@ -300,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bx.y[q] = -1;
           if (pg[q] == -2) continue;
           if (pg[q] < 0 || pg[q] >= a.pool_pages) {
-            flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+            if (rank == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
             continue;
           }
           const int64_t rho = rho0 + (int64_t)q * a.box_rows;
@@ -309,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto load_tile = [&](const Boxes& bx) -> bool {
-        for (int k = 0; k < kKSlots; ++k) {
+        for (int k = pp; k < kKSlots; k += 2) {
+          const uint32_t use = tile_base + k;
           const uint32_t slot = use % nslot;
           const uint32_t round = use / nslot;
           if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_s)) return false;
@@ -318,12 +347,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             unsigned char* dst = ring + slot * kChunkBytes;
             mbar_arrive_expect_tx(&full[slot], bx.bytes);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (bx.y[q] >= 0) tma_load_2d(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, bx.y[q]);
+            if ((k & 1) == (int)rank) {
+              // Exactly as many TMA instructions as boxes: issuing predicated-off
+              // copies in an unrolled loop still costs the producer issue time.
+              if (nbox == 1) {
+                if (bx.y[0] >= 0)
+                  tma_load_2d_multicast(dst, &tmap_kv, &full[slot], k * kChunkDims, bx.y[0], kBoth);
+              } else {
+                for (int q = 0; q < nbox; ++q) {
+                  const int32_t y = box_y(bx, q);
+                  if (y >= 0)
+                    tma_load_2d_multicast(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, y,
+                                          kBoth);
+                }
+              }
+            }
           }
-          ++use;
         }
+        tile_base += kKSlots;
         return true;
       };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
@@ -332,9 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
         int32_t pg_next[8];
         fetch_pages(b, nvis, t0, pg_next);
-        if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kQFull], Rg * 128);
-        tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 8 * kChunkDims, b * a.R_total + g * Rg);
+        if (pp == 0) {
+          if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars[kQFull], Rg * 128);
+          tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 8 * kChunkDims, b * a.R_total + g * Rg);
+        }
         ++seg;
         Boxes cur;
         make_boxes(rs, t0, pg_next, cur);
@@ -344,61 +387,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jj + 1 < nt) make_boxes(rs, t0 + jj + 1, pg_next, cur);
         }
       }
-      if (!ok) {
-        // drain: wait (bounded, ignoring the abort flag) for copies already issued
-        for (uint32_t k = 0; k < (uint32_t)nslot && k < use; ++k) {
-          const uint32_t uu = use - 1 - k;
-          const uint32_t slot = uu % nslot;
-          const uint64_t t0n = globaltimer();
-          while (!mbar_try_wait(&full[slot], (uu / nslot) & 1) && globaltimer() - t0n < kWaitLimitNs) {
-          }
+      // Drain: every release addressed to this CTA's ring (including the peer's
+      // remote ones) lands before the cluster may retire.  Bounded; skipped
+      // after an abort.
+      if (ok) {
+        const uint32_t total = ntiles_cta * kKSlots;
+        for (uint32_t s = pp; s < (uint32_t)nslot && s < total; s += 2) {
+          const uint32_t last = s + ((total - 1 - s) / nslot) * nslot;  // last use of slot s
+          if (!mbar_wait(&empty[s], (last / nslot) & 1, abort_s)) break;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // Event-driven single thread: QK chunks are issued as their data lands and
-    // each PV product as soon as its P tile is ready, so a PV never waits behind
-    // the next tile's loads (the PV releases the ring slots those loads need).
+    // each PV product as soon as its P tile is ready.
     if (lane == 0 && lo < hi) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, Rg, 1, 0);
-      // descriptor templates; a byte offset is added to the start-address field (>> 4)
       const uint64_t kdesc0 = sw128_desc(smem_u32(ring), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
       const uint64_t qrdesc0 = sw128_desc(smem_u32(qr_s), 16, 1024);
       const uint64_t pdesc0 = sw128_desc(smem_u32(p_s), 16, 1024);
+      const int my_lo = 4 * (int)rank;  // value chunks this CTA keeps for its PV product
+      const uint32_t peer_empty0 = mapa_shared(smem_u32(&empty[0]), peer);
+      auto release_both = [&](uint32_t slot) {  // plain arrive on both CTAs' empty[slot]
+        mbar_arrive(&empty[slot]);
+        mbar_arrive_cluster(peer_empty0 + slot * 8);
+      };
       auto issue_qk_chunk = [&](uint32_t j, int k, uint32_t slot) {
-        const uint32_t d = tmem + 4 * Rg + kTile * (j % nsbuf);
+        const uint32_t d = tmem + 2 * Rg + kTile * (j % nsbuf);
         const uint64_t kd = kdesc0 + ((slot * kChunkBytes) >> 4);
         if (k < 8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ts(d, tmem + kQTmemCol + k * 32 + kk * 8, kd + kk * 2, idesc_qk, (k | kk) != 0);
+          if (k < my_lo || k >= my_lo + 4) mma_commit_multicast(&empty[slot], kBoth);  // not one of my V chunks
         } else if (k == 8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + kk * 2, kd + kk * 2, idesc_qk, 1);
-          mma_commit(&empty[slot]);  // the rope chunk is not needed by the PV product
+          mma_commit_multicast(&empty[slot], kBoth);
         } else {
-          mbar_arrive(&empty[slot]);
+          release_both(slot);
         }
       };
       auto issue_pv = [&](uint32_t j, bool first) {
         const int pb = j & 1;
         const uint64_t pd = pdesc0 + ((pb * Rg * 128) >> 4);
-        const uint32_t base = j * kKSlots;
-        for (int t = 0; t < 4; ++t) {
+        const uint32_t base = j * kKSlots + my_lo;
+        for (int t = 0; t < 2; ++t) {
           const uint32_t slot = (base + 2 * t) % nslot;  // even: the pair (2t, 2t+1) is contiguous
           const uint64_t vd = vdesc0 + ((slot * kChunkBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ss(tmem + t * Rg, vd + kk * (2048 >> 4), pd + kk * 2, idesc_pv, !(first && kk == 0));
-          mma_commit(&empty[slot]);
-          mma_commit(&empty[slot + 1]);
+          mma_commit_multicast(&empty[slot], kBoth);
+          mma_commit_multicast(&empty[slot + 1], kBoth);
         }
         mma_commit(&bars[kPFree0 + pb]);
       };
-      // QK cursor
       SegIter itq;
       itq.init(a.tile_start, U, lo, hi);
       int32_t uq, t0q, ntq, ksq;
@@ -407,7 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_seg = 0, q_jj = 0, q_k = 0;
       bool q_seg_ready = false, q_tile_ready = false;
       uint32_t jq = 0;
-      // PV cursor
       SegIter itp;
       itp.init(a.tile_start, U, lo, hi);
       int32_t up, t0p, ntp, ksp;
@@ -416,11 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int p_seg = 0, p_jj = 0;
       uint32_t jp = 0;
       uint64_t idle_since = 0;
+      uint32_t idle_polls = 0;
       while (q_has || p_has) {
         bool progress = false;
         if (p_has && jp < jq) {
-          bool ready = mbar_try_wait(&bars[kPFull0 + (jp & 1)], (jp >> 1) & 1);
-          if (ready && p_jj == 0 && p_seg >= 1) ready = mbar_try_wait(&bars[kOFree], (p_seg - 1) & 1);
+          bool ready = mbar_test(&bars[kPFull0 + (jp & 1)], (jp >> 1) & 1);
+          if (ready && p_jj == 0 && p_seg >= 1) ready = mbar_test(&bars[kOFree], (p_seg - 1) & 1);
           if (ready) {
             tc_fence_after();
             issue_pv(jp, p_jj == 0);
@@ -434,12 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (q_has) {
-          if (!q_seg_ready && mbar_try_wait(&bars[kQFull], q_seg & 1)) {
+          if (!q_seg_ready && mbar_test(&bars[kQFull], q_seg & 1)) {
             q_seg_ready = true;
             progress = true;
           }
           if (q_seg_ready && !q_tile_ready &&
-              mbar_try_wait(&bars[kSFree0 + (jq % nsbuf)], ((jq / nsbuf) & 1) ^ 1)) {
+              mbar_test(&bars[kSFree0 + (jq % nsbuf)], ((jq / nsbuf) & 1) ^ 1)) {
             q_tile_ready = true;
             progress = true;
           }
@@ -447,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (q_k < kKSlots) {
               const uint32_t use = jq * kKSlots + q_k;
               const uint32_t slot = use % nslot;
-              if (!mbar_try_wait(&full[slot], (use / nslot) & 1)) break;
+              if (!mbar_test(&full[slot], (use / nslot) & 1)) break;
               tc_fence_after();
               issue_qk_chunk(jq, q_k, slot);
               ++q_k;
@@ -470,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (progress) {
           idle_since = 0;
-        } else {
+          idle_polls = 0;
+        } else if ((++idle_polls & 31) == 0) {  // look at the clock every 32 idle polls
           if (*abort_s) break;
           const uint64_t now = globaltimer();
           if (idle_since == 0) {
@@ -484,14 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ Q load, softmax, epilogue
-    // All waits here are warp-uniform (every lane waits, then __all_sync), and the
-    // four warps meet only through bounded mbarriers, so a timeout anywhere
-    // drains every thread instead of stranding some at a barrier.
+    // Waits are polled by one lane per warp and broadcast; the four warps meet
+    // only through bounded mbarriers, so a timeout drains every thread.
     const int c = 32 * (warp & 3) + lane;        // TMEM lane: query row (S, Q) / value dim (O^T)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     if (lo < hi) {
-      // one lane polls the barrier (128 spinning lanes would crowd the producer's
-      // TMA and barrier traffic); the warp then synchronises on its result
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
         int r = 1;
         if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
@@ -499,7 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         return r != 0;
       };
       uint32_t gphase = 0;  // kGroup phases passed
-      // every softmax warp arrives; returns the OR of the warps' flags
       auto group_sync = [&](bool flag_in, bool* any) -> bool {
         const bool wany = __any_sync(0xffffffffu, flag_in);
         if (lane == 0) vote_s[(gphase & 1) * 4 + (warp & 3)] = wany ? 1 : 0;
@@ -518,9 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t jglob = 0;
       int seg = 0;
       bool ok = true;
-      // PV #k (0-based, in this CTA's tile order) completes phase k/2 of p_free[k % 2].
-      // That barrier cannot run two phases ahead of this wait (its next phase needs
-      // P of tile k + 2, which this thread has not written), so the parity is exact.
+      // PV #k completes phase k/2 of p_free[k % 2]; that barrier cannot run two
+      // phases ahead of this wait (its next phase needs P of tile k + 2).
       auto wait_pv = [&](uint32_t k) -> bool { return wwait(&bars[kPFree0 + (k & 1)], (k >> 1) & 1); };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
         const int b = u / a.n_held, rs = u % a.n_held;
@@ -556,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wwait(&bars[kSFull0 + sb], (jglob / nsbuf) & 1)) { ok = false; break; }
           tc_fence_after();
           uint32_t sr[64];
-          tmem_ld32(tmem + lane_base + 4 * Rg + kTile * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(tmem + lane_base + 4 * Rg + kTile * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld32(tmem + lane_base + 2 * Rg + kTile * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(tmem + lane_base + 2 * Rg + kTile * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
@@ -592,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O^T columns of the rows whose maximum moved are scaled by alpha
             if (!wait_pv(jglob - 1)) { ok = false; break; }
             tc_fence_after();
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 2; ++t) {
               for (int c0 = 0; c0 < Rg; c0 += 16) {
                 uint32_t r[16];
                 const uint32_t addr = tmem + lane_base + t * Rg + c0;
@@ -634,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars[kPFull0 + pb]);
         }
         if (!ok) break;
-        // ---------------- epilogue: O^T (dims x rows) / l -> o, lse
+        // ---------------- epilogue: O^T (my dims x rows) / l -> o, lse
         if (!wait_pv(jglob - 1)) { ok = false; break; }
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -646,12 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int R_here = min(Rg, a.R_total - g * Rg);
         const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total + g * Rg;
         const int64_t piece = (int64_t)(2 * v + kslot) * a.R_total + g * Rg;
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < 2; ++t) {
           for (int c0 = 0; c0 < Rg; c0 += 16) {
             uint32_t r[16];
             tmem_ld16(tmem + lane_base + t * Rg + c0, r);
             tmem_ld_wait();
-            const int dim = t * 128 + c;
+            const int dim = 256 * (int)rank + t * 128 + c;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int row = c0 + i;
@@ -669,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (c < R_here) {
+        if (c < R_here && rank == 0) {
           if (whole)
             a.lse_part[out_row0 + c] = a.base2 ? lse2 : lse2 * kLn2;
           else
@@ -685,6 +728,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_s && tid == 0) flag(a.status, DCP_STATUS_TIMEOUT);
   tc_fence_before();
   __syncthreads();
+  // The peer may still have copies or arrivals addressed to this CTA's shared
+  // memory; retire the pair together.  After an abort, allow in-flight tensor
+  // core commits (microseconds) to land first.
+  if (*abort_s) __nanosleep(100000);
+  cluster_sync();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
@@ -775,6 +823,30 @@ int sm_count_current() {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int max_active_clusters(size_t smem) {
+  static size_t cached_smem = 0;
+  static int cached = -1, cached_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cached >= 0 && cached_smem == smem && cached_dev == dev) return cached;
+  if (cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 512, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, partial_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached = n;
+  cached_smem = smem;
+  cached_dev = dev;
+  return n;
+}
+
 bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, Plan* p) {
   const int R_total = q_len * H;
   p->ngroups = (R_total + kMaxGroupRows - 1) / kMaxGroupRows;
@@ -782,7 +854,7 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   p->Rg = ((per + 15) / 16) * 16;
   const int sms = sm_count_current();
   if (sms <= 0) return false;
-  p->V = sms / p->ngroups;
+  p->V = (sms / 2) / p->ngroups;  // ranges: one 2-CTA cluster per (range, row group)
   if (p->V < 1) p->V = 1;
   const SmemLayout base = smem_layout(p->Rg, 0);
   const size_t budget = 232448 - 1024;  // 227 KB minus alignment slack
@@ -790,8 +862,14 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   nslot &= ~1;
   if (nslot > kMaxSlots) nslot = kMaxSlots;
   p->nslot = nslot;
-  p->nsbuf = (4 * p->Rg + 2 * kTile <= kQTmemCol) ? 2 : 1;
+  p->nsbuf = (2 * p->Rg + 2 * kTile <= kQTmemCol) ? 2 : 1;
   p->smem = smem_layout(p->Rg, nslot).total + 1024;
+  // clusters that can be resident at once (both CTAs of a cluster share a GPC)
+  const int clusters = max_active_clusters(p->smem);
+  if (clusters > 0) {
+    p->V = clusters / p->ngroups;
+    if (p->V < 1) p->V = 1;
+  }
   const int P = layout->page_size;
   p->box_rows = P >= kTile ? kTile : P;
   const int64_t U = (int64_t)B * n_held;
@@ -906,7 +984,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   cudaStream_t st = as_stream(stream);
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
-  partial_tc_kernel<<<p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, a);
+  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, a);
   fixup_kernel<<<U, 256, 0, st>>>(a);
   return launch_status(3);
 }
