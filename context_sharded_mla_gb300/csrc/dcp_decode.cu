@@ -48,10 +48,11 @@ namespace {
 
 constexpr int kTile = 64;          // KV rows per tile
 constexpr int kChunkDims = 64;     // dims per chunk (one 128-byte swizzle row)
-constexpr int kNumChunks = 9;      // 576 / 64
 constexpr int kChunkBytes = kTile * 128;
-constexpr int kKSlots = 10;        // ring uses per tile (9 chunks + 1 unused: V chunk pairs start on even slots)
-constexpr int kMaxSlots = 26;
+constexpr int kKSlots = 8;         // main-ring uses per tile: chunks 0-7 (the value dims); pairs start on even slots
+constexpr int kMaxSlots = 28;
+constexpr int kRopeSlots = 3;      // separate small ring for chunk 8 (the 64 rope dims)
+constexpr int kTileBars = 4;       // per-tile "all chunks landed" barriers (> ring depth in tiles)
 constexpr int kQTmemCol = 256;     // TMEM columns [256, 512): query dims 0-511 as bf16 pairs
 constexpr int kThreads = 224;     // 7 warps: 2 producers, 1 MMA issuer, 4 softmax/epilogue
 constexpr int kProducerWarpB = 6;
@@ -85,19 +86,20 @@ struct TcArgs {
 };
 
 struct SmemLayout {
-  uint32_t q, ring, p, alpha, inv, vote, bars, misc, total;
+  uint32_t q, ring, rope, p, alpha, inv, vote, bars, misc, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int Rg, int nslot) {
   SmemLayout s;
   s.q = 0;                          // rope dims of the query rows: [Rg][64] bf16
   s.ring = Rg * 128;
-  s.p = s.ring + nslot * kChunkBytes;
+  s.rope = s.ring + nslot * kChunkBytes;
+  s.p = s.rope + kRopeSlots * kChunkBytes;
   s.alpha = s.p + 2 * Rg * 128;
   s.inv = s.alpha + 2 * 128 * 4;
   s.vote = s.inv + 2 * 128 * 4;
   s.bars = s.vote + 64;
-  s.misc = s.bars + (2 * kMaxSlots + 16) * 8;
+  s.misc = s.bars + (2 * kMaxSlots + 2 * kRopeSlots + kTileBars + 16) * 8;
   s.total = s.misc + 64;
   return s;
 }
@@ -227,8 +229,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float* inv_s = reinterpret_cast<float*>(smem + sl.inv);                  // [2][128]
   volatile int* vote_s = reinterpret_cast<volatile int*>(smem + sl.vote);  // [2][4]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
-  uint64_t* full = bars + kNumFixedBars;
-  uint64_t* empty = full + kMaxSlots;
+  uint64_t* empty = bars + kNumFixedBars;
+  uint64_t* rempty = empty + kMaxSlots;  // rope ring releases
+  uint64_t* tfull = rempty + kRopeSlots;  // all 9 chunks of a tile landed in this CTA
+  unsigned char* rope = smem + sl.rope;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + sl.misc);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + sl.misc + 4);
 
@@ -236,7 +240,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
   const int cid = blockIdx.x >> 1;  // cluster index
   const int v = cid / a.ngroups;
   const int g = cid % a.ngroups;
@@ -256,14 +259,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kPFull1], 4);
     mbar_init(&bars[kOFree], 4);
     mbar_init(&bars[kGroup], 4);
-    for (int i = 0; i < nslot; ++i) {
-      mbar_init(&full[i], 1);    // own producer's expect_tx; bytes from both CTAs' copies
-      mbar_init(&empty[i], 2);   // released by both CTAs' MMA issuers
-    }
+    for (int i = 0; i < nslot; ++i) mbar_init(&empty[i], 2);  // released by both CTAs' MMA issuers
+    for (int i = 0; i < kRopeSlots; ++i) mbar_init(&rempty[i], 2);
+    for (int i = 0; i < kTileBars; ++i) mbar_init(&tfull[i], 2);  // one arrive (with its bytes) per producer
     fence_barrier_init();
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
-  for (int i = tid; i < nslot * kChunkBytes / 16; i += kThreads)
+  for (int i = tid; i < (nslot + kRopeSlots) * kChunkBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -336,35 +338,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bx.bytes += a.box_rows * 128;
         }
       };
+      // one chunk (all its boxes) into `dst`, completing on `bar`, multicast to both CTAs
+      auto issue_chunk = [&](const Boxes& bx, unsigned char* dst, uint64_t* bar, int k) {
+        // exactly as many TMA instructions as boxes: predicated-off copies in an
+        // unrolled loop still cost the producer issue time
+        if (nbox == 1) {
+          if (bx.y[0] >= 0) tma_load_2d_multicast(dst, &tmap_kv, bar, k * kChunkDims, bx.y[0], kBoth);
+        } else {
+          for (int q = 0; q < nbox; ++q) {
+            const int32_t y = box_y(bx, q);
+            if (y >= 0) tma_load_2d_multicast(dst + q * a.box_rows * 128, &tmap_kv, bar, k * kChunkDims, y, kBoth);
+          }
+        }
+      };
+      uint32_t rope_use = 0, tile_idx = 0;
+      // Every chunk of a tile completes on the tile's barrier tfull[j % kTileBars]
+      // (both producers arrive once with the bytes of their chunks, whichever CTA
+      // copies them), so the MMA issuer waits once per tile and issues the whole
+      // QK product back to back.
       auto load_tile = [&](const Boxes& bx) -> bool {
+        uint64_t* tb = &tfull[tile_idx % kTileBars];
+        uint32_t slots[4];
+        int n = 0;
         for (int k = pp; k < kKSlots; k += 2) {
           const uint32_t use = tile_base + k;
           const uint32_t slot = use % nslot;
-          const uint32_t round = use / nslot;
-          if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_s)) return false;
-          if (k >= kNumChunks) {
-            mbar_arrive(&full[slot]);
-          } else {
-            unsigned char* dst = ring + slot * kChunkBytes;
-            mbar_arrive_expect_tx(&full[slot], bx.bytes);
-            if ((k & 1) == (int)rank) {
-              // Exactly as many TMA instructions as boxes: issuing predicated-off
-              // copies in an unrolled loop still costs the producer issue time.
-              if (nbox == 1) {
-                if (bx.y[0] >= 0)
-                  tma_load_2d_multicast(dst, &tmap_kv, &full[slot], k * kChunkDims, bx.y[0], kBoth);
-              } else {
-                for (int q = 0; q < nbox; ++q) {
-                  const int32_t y = box_y(bx, q);
-                  if (y >= 0)
-                    tma_load_2d_multicast(dst + q * a.box_rows * 128, &tmap_kv, &full[slot], k * kChunkDims, y,
-                                          kBoth);
-                }
-              }
-            }
-          }
+          if (!mbar_wait(&empty[slot], ((use / nslot) & 1) ^ 1, abort_s)) return false;
+          slots[n++] = slot;
+        }
+        uint32_t rslot = 0;
+        if (pp == 0) {
+          rslot = rope_use % kRopeSlots;
+          if (!mbar_wait(&rempty[rslot], ((rope_use / kRopeSlots) & 1) ^ 1, abort_s)) return false;
+          ++rope_use;
+        }
+        mbar_arrive_expect_tx(tb, bx.bytes * (pp == 0 ? 5 : 4));
+        if ((int)rank == pp) {  // this CTA copies the chunks of its parity (rank 0 also the rope chunk)
+          for (int i = 0; i < n; ++i) issue_chunk(bx, ring + slots[i] * kChunkBytes, tb, pp + 2 * i);
+          if (pp == 0) issue_chunk(bx, rope + rslot * kChunkBytes, tb, 8);
         }
         tile_base += kKSlots;
+        ++tile_idx;
         return true;
       };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
@@ -396,6 +410,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t last = s + ((total - 1 - s) / nslot) * nslot;  // last use of slot s
           if (!mbar_wait(&empty[s], (last / nslot) & 1, abort_s)) break;
         }
+        if (pp == 0) {
+          for (uint32_t s = 0; s < (uint32_t)kRopeSlots && s < ntiles_cta; ++s) {
+            const uint32_t last = s + ((ntiles_cta - 1 - s) / kRopeSlots) * kRopeSlots;
+            if (!mbar_wait(&rempty[s], (last / kRopeSlots) & 1, abort_s)) break;
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -410,25 +430,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t qrdesc0 = sw128_desc(smem_u32(qr_s), 16, 1024);
       const uint64_t pdesc0 = sw128_desc(smem_u32(p_s), 16, 1024);
       const int my_lo = 4 * (int)rank;  // value chunks this CTA keeps for its PV product
-      const uint32_t peer_empty0 = mapa_shared(smem_u32(&empty[0]), peer);
-      auto release_both = [&](uint32_t slot) {  // plain arrive on both CTAs' empty[slot]
-        mbar_arrive(&empty[slot]);
-        mbar_arrive_cluster(peer_empty0 + slot * 8);
-      };
+      const uint64_t rdesc0 = sw128_desc(smem_u32(rope), 16, 1024);
+      // QK product of chunk k (< 8: value dims from the main ring; 8: rope dims)
       auto issue_qk_chunk = [&](uint32_t j, int k, uint32_t slot) {
         const uint32_t d = tmem + 2 * Rg + kTile * (j % nsbuf);
-        const uint64_t kd = kdesc0 + ((slot * kChunkBytes) >> 4);
         if (k < 8) {
+          const uint64_t kd = kdesc0 + ((slot * kChunkBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ts(d, tmem + kQTmemCol + k * 32 + kk * 8, kd + kk * 2, idesc_qk, (k | kk) != 0);
           if (k < my_lo || k >= my_lo + 4) mma_commit_multicast(&empty[slot], kBoth);  // not one of my V chunks
-        } else if (k == 8) {
+        } else {
+          const uint64_t kd = rdesc0 + ((slot * kChunkBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + kk * 2, kd + kk * 2, idesc_qk, 1);
-          mma_commit_multicast(&empty[slot], kBoth);
-        } else {
-          release_both(slot);
+          mma_commit_multicast(&rempty[slot], kBoth);
         }
       };
       auto issue_pv = [&](uint32_t j, bool first) {
@@ -451,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int32_t uq, t0q, ntq, ksq;
       bool wq;
       bool q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
-      int q_seg = 0, q_jj = 0, q_k = 0;
+      int q_seg = 0, q_jj = 0;
       bool q_seg_ready = false, q_tile_ready = false;
       uint32_t jq = 0;
       SegIter itp;
@@ -463,6 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t jp = 0;
       uint64_t idle_since = 0;
       uint32_t idle_polls = 0;
+      uint32_t m_slot = 0, r_slot = 0;  // next main-ring and rope-ring slots the QK cursor reads
       while (q_has || p_has) {
         bool progress = false;
         if (p_has && jp < jq) {
@@ -490,29 +507,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             q_tile_ready = true;
             progress = true;
           }
-          if (q_tile_ready) {
-            while (q_k < kKSlots) {
-              const uint32_t use = jq * kKSlots + q_k;
-              const uint32_t slot = use % nslot;
-              if (!mbar_test(&full[slot], (use / nslot) & 1)) break;
-              tc_fence_after();
-              issue_qk_chunk(jq, q_k, slot);
-              ++q_k;
-              progress = true;
+          if (q_tile_ready && mbar_test(&tfull[jq % kTileBars], (jq / kTileBars) & 1)) {
+            // all 9 chunks of tile jq have landed: the whole QK product back to back
+            tc_fence_after();
+            for (int k = 0; k < kKSlots; ++k) {
+              issue_qk_chunk(jq, k, m_slot);
+              if (++m_slot == (uint32_t)nslot) m_slot = 0;
             }
-            if (q_k == kKSlots) {
-              mma_commit(&bars[kSFull0 + (jq % nsbuf)]);
-              if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
-              ++jq;
-              q_k = 0;
-              q_tile_ready = false;
-              if (++q_jj == ntq) {
-                ++q_seg;
-                q_jj = 0;
-                q_seg_ready = false;
-                q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
-              }
+            issue_qk_chunk(jq, kKSlots, r_slot);
+            if (++r_slot == (uint32_t)kRopeSlots) r_slot = 0;
+            mma_commit(&bars[kSFull0 + (jq % nsbuf)]);
+            if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
+            ++jq;
+            q_tile_ready = false;
+            if (++q_jj == ntq) {
+              ++q_seg;
+              q_jj = 0;
+              q_seg_ready = false;
+              q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
             }
+            progress = true;
           }
         }
         if (progress) {
