@@ -25,10 +25,12 @@ __all__ = [
     "DcpError", "Layout", "load_library", "library_path",
     "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
     "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count",
+    "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes",
     "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
 ]
 
 DCP_OK, DCP_ERR_INVALID, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA, DCP_ERR_WORKSPACE = 0, -1, -2, -3, -4
+DCP_ERR_TOO_LARGE = -5
 DCP_LSE_BASE_E, DCP_LSE_BASE_2 = 0, 1
 DCP_F32, DCP_BF16 = 0, 1
 STATUS_BITS = {1: "BAD_POSITION", 2: "BAD_PAGE_INDEX", 4: "BAD_PAGE_ID", 8: "BAD_REQUEST", 16: "BAD_LENGTH",
@@ -66,6 +68,9 @@ _SIGNATURES = {
                                       _P, _F, _I32, _P, _I32, _P, _P, _SZ, _P, _P]),
     "dcp_mla_decode_workspace_size": (_SZ, [_LP, _I32, _I32, _I32, _I32, _I32]),
     "dcp_lse_merge": (_I32, [_I32, _I64, _P, _I32, _P, _I32, _P, _I32, _P, _P]),
+    "dcp_mla_decode_partial_static": (_I32, [_LP, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _I64, _I64,
+                                             _P, _F, _I32, _P, _I32, _P, _P, _P]),
+    "dcp_mla_decode_static_scratch_bytes": (_SZ, []),
 }
 
 
@@ -217,3 +222,34 @@ def dcp_lse_merge(o_part, lse_part, lse_base, o, lse=None, stream=None):
     _check("dcp_lse_merge", load_library().dcp_lse_merge(
         n, rows, _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), lse_base, _ptr(o), _dtype_code(o),
         _ptr(lse), _stream(stream)))
+
+
+def dcp_mla_decode_static_scratch_bytes() -> int:
+    """Bytes of the library's built-in scratch array (per device)."""
+    return int(load_library().dcp_mla_decode_static_scratch_bytes())
+
+
+def dcp_mla_decode_partial_static(layout, shard_begin, shard_end, q, arena, pool_pages, block_table, max_pages,
+                                  seq_lens, scale, lse_base, o_part, lse_part, status, stream=None):
+    """dcp_mla_decode_partial without a workspace, for callers that cannot allocate device memory.
+
+    The library runs on its own built-in scratch array instead (one per device,
+    held until exit).  Its first call on a device does a one-time address lookup,
+    so make it before any stream capture; calls that overlap on the GPU share the
+    array and must be ordered.
+    """
+    B, q_len, H, dk = q.shape
+    n = shard_end - shard_begin
+    _dev(q, "q", torch.bfloat16, (B, q_len, H, 576))
+    _dev(arena, "arena", torch.bfloat16, (n, pool_pages * layout.page_size, 576))
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int64, (B,))
+    _dev(o_part, "o_part", o_part.dtype, (n, B, q_len, H, 512))
+    _dev(lse_part, "lse_part", torch.float32, (n, B, q_len, H))
+    _dev(status, "status", torch.int32, (1,))
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per request")
+    _check("dcp_mla_decode_partial_static", load_library().dcp_mla_decode_partial_static(
+        ctypes.byref(layout), shard_begin, shard_end, _ptr(q), B, q_len, H, _ptr(arena), pool_pages,
+        _ptr(block_table), block_table.shape[1], max_pages, _ptr(seq_lens), float(scale), lse_base,
+        _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))

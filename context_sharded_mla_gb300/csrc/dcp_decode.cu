@@ -38,6 +38,8 @@
 // writes the tile prefix sums.
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "dcp_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -1001,4 +1003,55 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, a);
   fixup_kernel<<<U, 256, 0, st>>>(a);
   return launch_status(3);
+}
+
+// ---------------------------------------------------------------------------- allocation-free variant
+// Some callers cannot hand the library a workspace: a serving process that has
+// given every free byte of HBM to its KV pool and forbids further device
+// allocations, or a plain C host with no device-memory manager of its own.
+// For them the partial decode can run on a scratch area that the library owns:
+// a file-scope device array, created when the library is loaded on a device and
+// kept until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB per device
+__device__ __align__(256) unsigned char g_partial_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_partial_scratch on the current device (looked up once per
+// device; in host code the array's name is only a host-side stand-in).
+void* scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_partial_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t dcp_mla_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" int32_t dcp_mla_decode_partial_static(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                                                 const void* q, int32_t B, int32_t q_len, int32_t H,
+                                                 const void* arena, int64_t pool_pages,
+                                                 const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                                                 const int64_t* seq_lens, float scale, int32_t lse_base,
+                                                 void* o_part, int32_t o_part_dtype, float* lse_part,
+                                                 int32_t* status, void* stream) {
+  const size_t need = dcp_mla_decode_workspace_size(layout, shard_begin, shard_end, B, q_len, H);
+  if (need == 0) return DCP_ERR_INVALID;
+  if (need > kStaticScratchBytes) return DCP_ERR_TOO_LARGE;
+  void* ws = scratch_address();
+  if (!ws) return DCP_ERR_CUDA;
+  return dcp_mla_decode_partial(layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages, block_table,
+                                bt_stride, max_pages, seq_lens, scale, lse_base, o_part, o_part_dtype, lse_part, ws,
+                                kStaticScratchBytes, status, stream);
 }

@@ -27,6 +27,7 @@ extern "C" const char* dcp_error_string(int32_t code) {
     case DCP_ERR_UNSUPPORTED: return "unsupported configuration";
     case DCP_ERR_CUDA: return "CUDA call failed";
     case DCP_ERR_WORKSPACE: return "workspace missing or too small";
+    case DCP_ERR_TOO_LARGE: return "sizes need more scratch than the built-in area";
     default: return "unknown error";
   }
 }

@@ -63,7 +63,8 @@ enum {
   DCP_ERR_INVALID = -1,      /* bad argument (null pointer, size, layout, dtype) */
   DCP_ERR_UNSUPPORTED = -2,  /* valid but outside what this build handles */
   DCP_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed */
-  DCP_ERR_WORKSPACE = -4     /* workspace missing or smaller than required */
+  DCP_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required */
+  DCP_ERR_TOO_LARGE = -5     /* sizes need more scratch than the library's built-in area */
 };
 
 /* Device status bits (OR-ed into *status). */
@@ -223,6 +224,39 @@ size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int32_t shard_b
 int32_t dcp_lse_merge(int32_t n_parts, int64_t rows, const void* o_part, int32_t o_part_dtype,
                       const float* lse_part, int32_t lse_base, void* o, int32_t o_dtype,
                       float* lse, void* stream);
+
+/*
+ * dcp_mla_decode_partial_static — dcp_mla_decode_partial without a caller workspace.
+ *
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory for a workspace — a serving process that has given all
+ * free HBM to its KV pool and allows no further allocations, or a plain C host
+ * program with no device-memory manager.  It computes exactly what
+ * dcp_mla_decode_partial computes, with the same arguments minus the workspace,
+ * and allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * Scratch comes from a file-scope device array of
+ * dcp_mla_decode_static_scratch_bytes() bytes (64 MiB) that every GPU holds from
+ * the moment it loads this library until the process exits.  The first call on
+ * a device looks up that array's device address (cudaGetSymbolAddress, with the
+ * device current); make that first call before any stream capture.  Every call
+ * on a device shares the one array and leaves its contents behind; nothing in it
+ * has to start at zero.  Calls whose work overlaps on the GPU (different streams,
+ * or different host threads without ordering) race on the array and give wrong
+ * results: order them.
+ * Errors: as dcp_mla_decode_partial, plus DCP_ERR_TOO_LARGE when
+ * dcp_mla_decode_workspace_size(...) for these sizes exceeds the array.
+ */
+int32_t dcp_mla_decode_partial_static(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                                      const void* q, int32_t B, int32_t q_len, int32_t H,
+                                      const void* arena, int64_t pool_pages,
+                                      const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                                      const int64_t* seq_lens, float scale, int32_t lse_base,
+                                      void* o_part, int32_t o_part_dtype, float* lse_part,
+                                      int32_t* status, void* stream);
+
+/* Size in bytes of the built-in scratch array dcp_mla_decode_partial_static uses. */
+size_t dcp_mla_decode_static_scratch_bytes(void);
 
 #ifdef __cplusplus
 }
