@@ -223,6 +223,7 @@ def run_ours(args, cfg, rank, world, dist, device):
     launches0 = dcp.dcp_launch_count()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()           # bounds an `ncu --profile-from-start off` launch list
     t0.record(stream)
     for i in range(args.steps):
         ev_step[i][0].record(stream)
@@ -230,6 +231,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         ev_step[i][1].record(stream)
     t1.record(stream)
     barrier(dist)
+    torch.cuda.profiler.stop()
     launches = dcp.dcp_launch_count() - launches0
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)

@@ -9,26 +9,31 @@
 // "DCP x speculative decoding" (causal mask in global positions, from the shard
 // rank and the global lengths).
 //
-// Design: persistent 2-CTA clusters (one CTA per SM, 192 threads each):
-//   warp 0      TMA producer: the 64 rope dims of the query rows once per
-//               segment; KV tiles of 64 local rows x 64 dims ("chunks", 8 KB,
-//               128-byte swizzle) into a ring of ~22 chunk slots.  Each chunk is
-//               fetched once and multicast into both CTAs of the cluster.
+// Design: persistent 2-CTA clusters, one CTA per SM, 192 threads each:
+//   warp 0      TMA producer: this CTA's share of every KV tile (64 local rows)
+//               into a ring of tile slots, and (CTA 0) the query's 64 rope dims
+//               once per segment.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
-//   warps 2-5   load the 512 c_K dims of the query rows into TMEM once per
+//   warps 2-5   load this CTA's half of the query's c_K dims into TMEM once per
 //               segment, then softmax (one query row per thread) and epilogue.
-// A cluster handles a group of at most 96 query rows.  Both CTAs compute the
-// same S and P; CTA r keeps value dims [256 r, 256 r + 256).  TMEM per CTA:
-// O^T (2 x 96 columns), one S tile (64) and the query's c_K part as the MMA A
-// operand (256 columns).  Per tile j:
-//   S_j   = Q K_j^T            M=128 rows (A: TMEM for dims 0-511, smem for the
-//                              64 rope dims), N=64 KV rows, K=576        -> TMEM fp32
-//   P_j   = exp2(S_j*scale*log2e - m)      online softmax with lazy rescaling
-//   O^T  += V_j^T P_j^T        M=128 value dims (x2), N=rows, K=64 KV rows -> TMEM fp32
-// The tile's chunks stay in the ring from the QK product to the PV product
-// (V = the first 512 dims of the same rows), so every KV byte crosses HBM once
-// and reaches each SM's shared memory once.  O is kept transposed (dims on
-// TMEM lanes) so the accumulator needs only 2 columns per query row per CTA.
+// A cluster handles a group of at most 128 query rows.  The 576 key dims are
+// split between the two CTAs: CTA r loads value chunks 4r .. 4r + 3 (dims
+// [256 r, 256 r + 256), 128-byte swizzled boxes of 64 rows x 64 dims) and CTA 0
+// also the rope chunk.  Per tile j, in each CTA:
+//   S_j^r = Q[:, K_r] K_j[:, K_r]^T   M=128 rows (A: TMEM; rope part from smem),
+//                                     N=64 KV rows, K=256 (+64)     -> TMEM fp32
+//   the two partial score tiles are swapped through distributed shared memory
+//   (st.async, credited on the receiver's mbarrier) and each CTA forms
+//   S_j = S_j^0 + S_j^1 (fp32 addition is commutative, so both CTAs hold the same
+//   bits and take the same softmax decisions);
+//   P_j   = exp2(S_j*scale*log2e - m)  online softmax with lazy rescaling,
+//                                     written back over S_j as bf16 pairs
+//   O_r  += P_j V_j[:, dims of r]     M=128 rows (A = P from TMEM), N=256,
+//                                     K=64 KV rows                   -> TMEM fp32
+// Each KV byte crosses HBM once and reaches one SM's shared memory once; the
+// tile's chunks stay in the ring from the QK product to the PV product (V = the
+// first 512 dims of the same rows).  TMEM per CTA: O (256 columns), two S/P
+// tiles (2 x 64) and the query's c_K half (128).
 //
 // Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
 // concatenation of all units' tiles is cut into V equal ranges, one per cluster
@@ -48,28 +53,28 @@ using namespace dcp::sm100;
 
 namespace {
 
-constexpr int kTile = 64;          // KV rows per tile
-constexpr int kChunkDims = 64;     // dims per chunk (one 128-byte swizzle row)
-constexpr int kChunkBytes = kTile * 128;
-constexpr int kKSlots = 8;         // main-ring uses per tile: chunks 0-7 (the value dims); pairs start on even slots
-constexpr int kMaxSlots = 28;
-constexpr int kRopeSlots = 3;      // separate small ring for chunk 8 (the 64 rope dims)
-constexpr int kTileBars = 4;       // per-tile "all chunks landed" barriers (> ring depth in tiles)
-constexpr int kQTmemCol = 256;     // TMEM columns [256, 512): query dims 0-511 as bf16 pairs
-constexpr int kThreads = 224;     // 7 warps: 2 producers, 1 MMA issuer, 4 softmax/epilogue
-constexpr int kProducerWarpB = 6;
+constexpr int kTile = 64;                     // KV rows per tile
+constexpr int kChunkDims = 64;                // dims per chunk (one 128-byte swizzle row)
+constexpr int kChunkBytes = kTile * 128;      // 8 KB
+constexpr int kOwnChunks = 4;                 // value chunks each CTA loads (256 dims)
+constexpr int kSlotBytes = kOwnChunks * kChunkBytes;
+constexpr int kMaxTileSlots = 8;
+constexpr int kThreads = 192;                 // 6 warps: producer, MMA issuer, 4 softmax/epilogue
+constexpr int kMaxGroupRows = 128;
+constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
+constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns (P over them)
+constexpr uint32_t kQCol = 384;               // [384, 512): the query's c_K half as bf16 pairs
+constexpr int kXRowBytes = kTile * 4;         // one row of a partial score tile (fp32)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
-constexpr int kMaxGroupRows = 96;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: P stays <= 256
 
 struct TcArgs {
   Layout L;
   int32_t shard_begin, n_held;
   int32_t B, q_len, H, R_total;  // R_total = q_len * H
   int32_t Rg, ngroups, V;        // rows per group, groups, stream-K ranges
-  int32_t nslot;
-  int32_t nsbuf;                 // S tiles in TMEM (1 or 2)
+  int32_t nts;                   // tile slots in the ring
   int32_t box_rows;              // KV TMA box height = min(P, 64)
   int64_t pool_rows, pool_pages;
   const int32_t* bt;
@@ -88,26 +93,25 @@ struct TcArgs {
 };
 
 struct SmemLayout {
-  uint32_t q, ring, rope, p, alpha, inv, vote, bars, misc, total;
+  uint32_t qr, x, ring, rope, bars, misc, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int Rg, int nslot) {
+__host__ __device__ inline uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
+
+__host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   SmemLayout s;
-  s.q = 0;                          // rope dims of the query rows: [Rg][64] bf16
-  s.ring = Rg * 128;
-  s.rope = s.ring + nslot * kChunkBytes;
-  s.p = s.rope + kRopeSlots * kChunkBytes;
-  s.alpha = s.p + 2 * Rg * 128;
-  s.inv = s.alpha + 2 * 128 * 4;
-  s.vote = s.inv + 2 * 128 * 4;
-  s.bars = s.vote + 64;
-  s.misc = s.bars + (2 * kMaxSlots + 2 * kRopeSlots + kTileBars + 16) * 8;
+  s.qr = 0;                                        // rope dims of the query rows: [128][64] bf16, swizzled
+  s.x = 128 * 128;                                 // the peer's partial scores: [Rg][64] fp32
+  s.ring = s.x + round1024((uint32_t)Rg * kXRowBytes);
+  s.rope = s.ring + nts * kSlotBytes;              // rope chunk of each tile slot (CTA 0)
+  s.bars = s.rope + nts * kChunkBytes;
+  s.misc = s.bars + (16 + 2 * kMaxTileSlots) * 8;
   s.total = s.misc + 64;
   return s;
 }
 
-enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPFree0, kPFree1, kOFree,
-           kGroup, kNumFixedBars };
+enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree, kXFull, kXEmpty,
+           kNumFixedBars };
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
   const int64_t S = a.seq_lens[b];
@@ -212,29 +216,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------------------- main kernel
-// A 2-CTA cluster per work range.  Both CTAs compute the same S and P for the
-// group's rows; CTA `rank` accumulates value dims [256 rank, 256 rank + 256)
-// (value chunks 4 rank .. 4 rank + 3).  Every KV chunk is fetched once and
-// multicast into both CTAs' rings (rank 0 issues the even chunks, rank 1 the odd
-// ones); a slot is refilled only when both CTAs have released it.
+// A 2-CTA cluster per (work range, row group).  CTA `rank` loads key/value dims
+// [256 rank, 256 rank + 256) of every tile (CTA 0 also the 64 rope dims),
+// computes its partial scores over them, swaps partial scores with its peer and
+// accumulates its own 256 value dims of O.  Both CTAs walk the same tile
+// sequence in lockstep through the score exchange.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
                       TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemLayout sl = smem_layout(a.Rg, a.nslot);
-  unsigned char* qr_s = smem + sl.q;
+  const SmemLayout sl = smem_layout(a.Rg, a.nts);
+  unsigned char* qr_s = smem + sl.qr;
+  unsigned char* x_s = smem + sl.x;
   unsigned char* ring = smem + sl.ring;
-  unsigned char* p_s = smem + sl.p;
-  float* alpha_s = reinterpret_cast<float*>(smem + sl.alpha);              // [2][128]
-  float* inv_s = reinterpret_cast<float*>(smem + sl.inv);                  // [2][128]
-  volatile int* vote_s = reinterpret_cast<volatile int*>(smem + sl.vote);  // [2][4]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
-  uint64_t* empty = bars + kNumFixedBars;
-  uint64_t* rempty = empty + kMaxSlots;  // rope ring releases
-  uint64_t* tfull = rempty + kRopeSlots;  // all 9 chunks of a tile landed in this CTA
   unsigned char* rope = smem + sl.rope;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
+  uint64_t* tfull = bars + 16;                  // tile slot landed
+  uint64_t* tempty = tfull + kMaxTileSlots;     // tile slot released by its PV product
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + sl.misc);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + sl.misc + 4);
 
@@ -246,65 +246,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int v = cid / a.ngroups;
   const int g = cid % a.ngroups;
   const int Rg = a.Rg;
-  const int nslot = a.nslot;
-  const int nsbuf = a.nsbuf;
+  const int nts = a.nts;
+  const int nact = (Rg + 31) >> 5;  // softmax warps holding at least one row of the group
   const int32_t U = a.B * a.n_held;
-  constexpr uint16_t kBoth = 0x3;
+  const int64_t T = a.tile_start[U];
+  const int64_t lo = range_lo(T, v, a.V), hi = range_lo(T, v + 1, a.V);
+  const uint32_t ntiles_cta = (uint32_t)(hi - lo);
 
   if (tid == 0) {
     *abort_s = 0;
     for (int i = 0; i < kNumFixedBars; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&bars[kQFull], 5);   // producer (rope TMA bytes) + 4 warps storing Q into TMEM
-    mbar_init(&bars[kSFree0], 4);
-    mbar_init(&bars[kSFree1], 4);
-    mbar_init(&bars[kPFull0], 4);
-    mbar_init(&bars[kPFull1], 4);
-    mbar_init(&bars[kOFree], 4);
-    mbar_init(&bars[kGroup], 4);
-    for (int i = 0; i < nslot; ++i) mbar_init(&empty[i], 2);  // released by both CTAs' MMA issuers
-    for (int i = 0; i < kRopeSlots; ++i) mbar_init(&rempty[i], 2);
-    for (int i = 0; i < kTileBars; ++i) mbar_init(&tfull[i], 2);  // one arrive (with its bytes) per producer
+    mbar_init(&bars[kQFull], nact + (rank == 0 ? 1 : 0));  // softmax warps (+ the rope TMA on CTA 0)
+    mbar_init(&bars[kPFull0], nact);
+    mbar_init(&bars[kPFull1], nact);
+    mbar_init(&bars[kOFree], nact);
+    mbar_init(&bars[kXEmpty], nact);  // remote arrivals: the peer's warps have read my scores
+    for (int i = 0; i < nts; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 1);
+    }
     fence_barrier_init();
+    // the peer's first partial tile is expected before it can be sent
+    if (ntiles_cta > 0) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
-  for (int i = tid; i < (nslot + kRopeSlots) * kChunkBytes / 16; i += kThreads)
+  for (int i = tid; i < nts * (kSlotBytes + kChunkBytes) / 16; i += kThreads)
     reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < 128 * 128 / 16; i += kThreads) reinterpret_cast<uint4*>(qr_s)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_base_s, 512);
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs exist before any multicast copy or remote arrive
+  cluster_sync();  // both CTAs' barriers exist before any remote store or arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
-  const int64_t T = a.tile_start[U];
-  const int64_t lo = range_lo(T, v, a.V), hi = range_lo(T, v + 1, a.V);
-  const uint32_t ntiles_cta = (uint32_t)(hi - lo);
-
-  if (warp == 0 || warp == kProducerWarpB) {
-    // ------------------------------------------------------------------ producers
-    // Two producer threads split each tile's ring uses by parity (producer pp
-    // handles chunks k = pp, pp + 2, ...), halving the per-use barrier/TMA
-    // latency chain; slot parity equals use parity, so each owns half the slots.
-    const int pp = warp == 0 ? 0 : 1;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
     if (lane == 0 && lo < hi) {
-      prefetch_tmap(&tmap_q);
+      if (rank == 0) prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_kv);
       SegIter it;
       it.init(a.tile_start, U, lo, hi);
       int32_t u, t0, nt, kslot;
       bool whole;
-      uint32_t tile_base = 0;  // first ring use of the current tile (kKSlots per tile)
+      uint32_t j = 0;  // tile index within this CTA's range
       int seg = 0;
       bool ok = true;
-      // page ids are fetched one tile ahead (raw loads consumed a tile later)
+      const int nbox = kTile / a.box_rows;
       struct Boxes {
         int32_t y[8];
         uint32_t bytes;
       };
-      const int nbox = kTile / a.box_rows;
       auto box_y = [](const Boxes& bx, int q) -> int32_t {  // register-resident select (no local memory)
         int32_t y = bx.y[0];
 #pragma unroll
@@ -312,6 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (q == i) y = bx.y[i];
         return y;
       };
+      // page ids are fetched one tile ahead (raw loads consumed a tile later)
       auto fetch_pages = [&](int b, int64_t nvis, int32_t tile, int32_t (&pg)[8]) {
         const int64_t rho0 = (int64_t)tile * kTile;
 #pragma unroll
@@ -340,47 +336,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bx.bytes += a.box_rows * 128;
         }
       };
-      // one chunk (all its boxes) into `dst`, completing on `bar`, multicast to both CTAs
+      // one chunk (all its boxes) into `dst`; exactly as many TMA instructions as
+      // boxes (predicated-off copies in an unrolled loop still cost issue time)
       auto issue_chunk = [&](const Boxes& bx, unsigned char* dst, uint64_t* bar, int k) {
-        // exactly as many TMA instructions as boxes: predicated-off copies in an
-        // unrolled loop still cost the producer issue time
         if (nbox == 1) {
-          if (bx.y[0] >= 0) tma_load_2d_multicast(dst, &tmap_kv, bar, k * kChunkDims, bx.y[0], kBoth);
+          if (bx.y[0] >= 0) tma_load_2d(dst, &tmap_kv, bar, k * kChunkDims, bx.y[0]);
         } else {
           for (int q = 0; q < nbox; ++q) {
             const int32_t y = box_y(bx, q);
-            if (y >= 0) tma_load_2d_multicast(dst + q * a.box_rows * 128, &tmap_kv, bar, k * kChunkDims, y, kBoth);
+            if (y >= 0) tma_load_2d(dst + q * a.box_rows * 128, &tmap_kv, bar, k * kChunkDims, y);
           }
         }
       };
-      uint32_t rope_use = 0, tile_idx = 0;
-      // Every chunk of a tile completes on the tile's barrier tfull[j % kTileBars]
-      // (both producers arrive once with the bytes of their chunks, whichever CTA
-      // copies them), so the MMA issuer waits once per tile and issues the whole
-      // QK product back to back.
+      const int nchunks = rank == 0 ? kOwnChunks + 1 : kOwnChunks;
       auto load_tile = [&](const Boxes& bx) -> bool {
-        uint64_t* tb = &tfull[tile_idx % kTileBars];
-        uint32_t slots[4];
-        int n = 0;
-        for (int k = pp; k < kKSlots; k += 2) {
-          const uint32_t use = tile_base + k;
-          const uint32_t slot = use % nslot;
-          if (!mbar_wait(&empty[slot], ((use / nslot) & 1) ^ 1, abort_s)) return false;
-          slots[n++] = slot;
-        }
-        uint32_t rslot = 0;
-        if (pp == 0) {
-          rslot = rope_use % kRopeSlots;
-          if (!mbar_wait(&rempty[rslot], ((rope_use / kRopeSlots) & 1) ^ 1, abort_s)) return false;
-          ++rope_use;
-        }
-        mbar_arrive_expect_tx(tb, bx.bytes * (pp == 0 ? 5 : 4));
-        if ((int)rank == pp) {  // this CTA copies the chunks of its parity (rank 0 also the rope chunk)
-          for (int i = 0; i < n; ++i) issue_chunk(bx, ring + slots[i] * kChunkBytes, tb, pp + 2 * i);
-          if (pp == 0) issue_chunk(bx, rope + rslot * kChunkBytes, tb, 8);
-        }
-        tile_base += kKSlots;
-        ++tile_idx;
+        const uint32_t ts = j % nts;
+        if (!mbar_wait(&tempty[ts], ((j / nts) & 1) ^ 1, abort_s)) return false;
+        mbar_arrive_expect_tx(&tfull[ts], bx.bytes * nchunks);
+        unsigned char* dst = ring + ts * kSlotBytes;
+        for (int i = 0; i < kOwnChunks; ++i)
+          issue_chunk(bx, dst + i * kChunkBytes, &tfull[ts], kOwnChunks * (int)rank + i);
+        if (rank == 0) issue_chunk(bx, rope + ts * kChunkBytes, &tfull[ts], 2 * kOwnChunks);
+        ++j;
         return true;
       };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
@@ -389,10 +366,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
         int32_t pg_next[8];
         fetch_pages(b, nvis, t0, pg_next);
-        if (pp == 0) {
+        if (rank == 0) {
           if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars[kQFull], Rg * 128);
-          tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 8 * kChunkDims, b * a.R_total + g * Rg);
+          tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 2 * kOwnChunks * kChunkDims, b * a.R_total + g * Rg);
         }
         ++seg;
         Boxes cur;
@@ -403,66 +380,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (jj + 1 < nt) make_boxes(rs, t0 + jj + 1, pg_next, cur);
         }
       }
-      // Drain: every release addressed to this CTA's ring (including the peer's
-      // remote ones) lands before the cluster may retire.  Bounded; skipped
-      // after an abort.
+      // Drain: every slot's last release (a tensor-core commit) lands before the
+      // CTA may retire.  Bounded; skipped after an abort.
       if (ok) {
-        const uint32_t total = ntiles_cta * kKSlots;
-        for (uint32_t s = pp; s < (uint32_t)nslot && s < total; s += 2) {
-          const uint32_t last = s + ((total - 1 - s) / nslot) * nslot;  // last use of slot s
-          if (!mbar_wait(&empty[s], (last / nslot) & 1, abort_s)) break;
-        }
-        if (pp == 0) {
-          for (uint32_t s = 0; s < (uint32_t)kRopeSlots && s < ntiles_cta; ++s) {
-            const uint32_t last = s + ((ntiles_cta - 1 - s) / kRopeSlots) * kRopeSlots;
-            if (!mbar_wait(&rempty[s], (last / kRopeSlots) & 1, abort_s)) break;
-          }
+        for (uint32_t s = 0; s < (uint32_t)nts && s < ntiles_cta; ++s) {
+          const uint32_t last = s + ((ntiles_cta - 1 - s) / nts) * nts;  // last tile in slot s
+          if (!mbar_wait(&tempty[s], (last / nts) & 1, abort_s)) break;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Event-driven single thread: QK chunks are issued as their data lands and
-    // each PV product as soon as its P tile is ready.
+    // Event-driven single thread.  Tensor-core operations issued by one thread
+    // run in issue order, so QK(j + 2) may be issued right after PV(j): it
+    // overwrites the S/P tile that PV(j) reads only after PV(j) has read it.
     if (lane == 0 && lo < hi) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, Rg, 1, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t kdesc0 = sw128_desc(smem_u32(ring), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
       const uint64_t qrdesc0 = sw128_desc(smem_u32(qr_s), 16, 1024);
-      const uint64_t pdesc0 = sw128_desc(smem_u32(p_s), 16, 1024);
-      const int my_lo = 4 * (int)rank;  // value chunks this CTA keeps for its PV product
       const uint64_t rdesc0 = sw128_desc(smem_u32(rope), 16, 1024);
-      // QK product of chunk k (< 8: value dims from the main ring; 8: rope dims)
-      auto issue_qk_chunk = [&](uint32_t j, int k, uint32_t slot) {
-        const uint32_t d = tmem + 2 * Rg + kTile * (j % nsbuf);
-        if (k < 8) {
-          const uint64_t kd = kdesc0 + ((slot * kChunkBytes) >> 4);
+      auto issue_qk = [&](uint32_t j) {
+        const uint32_t ts = j % nts;
+        const uint32_t d = tmem + kSCol + kTile * (j & 1);
+#pragma unroll
+        for (int i = 0; i < kOwnChunks; ++i) {
+          const uint64_t kd = kdesc0 + ((ts * kSlotBytes + i * kChunkBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(d, tmem + kQTmemCol + k * 32 + kk * 8, kd + kk * 2, idesc_qk, (k | kk) != 0);
-          if (k < my_lo || k >= my_lo + 4) mma_commit_multicast(&empty[slot], kBoth);  // not one of my V chunks
-        } else {
-          const uint64_t kd = rdesc0 + ((slot * kChunkBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + kk * 2, kd + kk * 2, idesc_qk, 1);
-          mma_commit_multicast(&rempty[slot], kBoth);
+            mma_bf16_ts(d, tmem + kQCol + 32 * i + 8 * kk, kd + 2 * kk, idesc_qk, (i | kk) != 0);
         }
+        if (rank == 0) {
+          const uint64_t rd = rdesc0 + ((ts * kChunkBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rd + 2 * kk, idesc_qk, 1);
+        }
+        mma_commit(&bars[kSFull0 + (j & 1)]);
       };
       auto issue_pv = [&](uint32_t j, bool first) {
-        const int pb = j & 1;
-        const uint64_t pd = pdesc0 + ((pb * Rg * 128) >> 4);
-        const uint32_t base = j * kKSlots + my_lo;
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t slot = (base + 2 * t) % nslot;  // even: the pair (2t, 2t+1) is contiguous
-          const uint64_t vd = vdesc0 + ((slot * kChunkBytes) >> 4);
+        const uint32_t ts = j % nts;
+        const uint32_t pa = tmem + kSCol + kTile * (j & 1);  // P: 64 bf16 = 32 columns
+        const uint64_t vd = vdesc0 + ((ts * kSlotBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + t * Rg, vd + kk * (2048 >> 4), pd + kk * 2, idesc_pv, !(first && kk == 0));
-          mma_commit_multicast(&empty[slot], kBoth);
-          mma_commit_multicast(&empty[slot + 1], kBoth);
-        }
-        mma_commit(&bars[kPFree0 + pb]);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(tmem + kOCol, pa + 8 * kk, vd + kk * (2048 >> 4), idesc_pv, !(first && kk == 0));
+        mma_commit(&tempty[ts]);
+        mma_commit(&bars[kPVDone0 + (j & 1)]);
       };
       SegIter itq;
       itq.init(a.tile_start, U, lo, hi);
@@ -470,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool wq;
       bool q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
       int q_seg = 0, q_jj = 0;
-      bool q_seg_ready = false, q_tile_ready = false;
+      bool q_seg_ready = false;
       uint32_t jq = 0;
       SegIter itp;
       itp.init(a.tile_start, U, lo, hi);
@@ -481,7 +445,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t jp = 0;
       uint64_t idle_since = 0;
       uint32_t idle_polls = 0;
-      uint32_t m_slot = 0, r_slot = 0;  // next main-ring and rope-ring slots the QK cursor reads
       while (q_has || p_has) {
         bool progress = false;
         if (p_has && jp < jq) {
@@ -499,29 +462,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
-        if (q_has) {
+        if (q_has && jq <= jp + 1) {  // the S/P tile of jq was last read by PV(jq - 2)
           if (!q_seg_ready && mbar_test(&bars[kQFull], q_seg & 1)) {
             q_seg_ready = true;
             progress = true;
           }
-          if (q_seg_ready && !q_tile_ready &&
-              mbar_test(&bars[kSFree0 + (jq % nsbuf)], ((jq / nsbuf) & 1) ^ 1)) {
-            q_tile_ready = true;
-            progress = true;
-          }
-          if (q_tile_ready && mbar_test(&tfull[jq % kTileBars], (jq / kTileBars) & 1)) {
-            // all 9 chunks of tile jq have landed: the whole QK product back to back
+          if (q_seg_ready && mbar_test(&tfull[jq % nts], (jq / nts) & 1)) {
             tc_fence_after();
-            for (int k = 0; k < kKSlots; ++k) {
-              issue_qk_chunk(jq, k, m_slot);
-              if (++m_slot == (uint32_t)nslot) m_slot = 0;
-            }
-            issue_qk_chunk(jq, kKSlots, r_slot);
-            if (++r_slot == (uint32_t)kRopeSlots) r_slot = 0;
-            mma_commit(&bars[kSFull0 + (jq % nsbuf)]);
+            issue_qk(jq);
             if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
             ++jq;
-            q_tile_ready = false;
             if (++q_jj == ntq) {
               ++q_seg;
               q_jj = 0;
@@ -546,29 +496,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------------ Q load, softmax, epilogue
-    // Waits are polled by one lane per warp and broadcast; the four warps meet
-    // only through bounded mbarriers, so a timeout drains every thread.
-    const int c = 32 * (warp & 3) + lane;        // TMEM lane: query row (S, Q) / value dim (O^T)
+  } else if (32 * (warp & 3) < Rg) {
+    // ------------------------------------------------------------------ Q load, score exchange, softmax, epilogue
+    // Waits are polled by one lane per warp and broadcast, so a timeout drains
+    // every thread.  A thread owns query row c (TMEM lane c) of the group.
+    const int c = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const bool has_x = c < Rg;  // this row's partial scores cross to the peer
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer) + (uint32_t)c * kXRowBytes;
+    const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull]), peer);
+    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty]), peer);
+    const uint4* x_mine = reinterpret_cast<const uint4*>(x_s + c * kXRowBytes);
     if (lo < hi) {
+      // Lane 0 polls (bounded) and broadcasts; on success every lane tests the
+      // completed phase once more, which gives each lane its own acquire.
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
         int r = 1;
         if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
         r = __shfl_sync(0xffffffffu, r, 0);
+        if (r) mbar_try_wait(bar, parity);
         return r != 0;
       };
-      uint32_t gphase = 0;  // kGroup phases passed
-      auto group_sync = [&](bool flag_in, bool* any) -> bool {
-        const bool wany = __any_sync(0xffffffffu, flag_in);
-        if (lane == 0) vote_s[(gphase & 1) * 4 + (warp & 3)] = wany ? 1 : 0;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kGroup]);
-        if (!wwait(&bars[kGroup], gphase & 1)) return false;
-        const int base = (gphase & 1) * 4;
-        *any = vote_s[base] | vote_s[base + 1] | vote_s[base + 2] | vote_s[base + 3];
-        ++gphase;
+      auto wwait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
+        int r = 1;
+        if (lane == 0) r = mbar_wait_cluster(bar, parity, abort_s) ? 1 : 0;
+        r = __shfl_sync(0xffffffffu, r, 0);
+        if (r) mbar_try_wait_cluster(bar, parity);
+        return r != 0;
+      };
+      // Scores of tile j: read this CTA's partial from TMEM and send it to the
+      // peer (16-byte pieces, 128-byte rows swizzled by row so a warp's stores
+      // spread over all banks).
+      auto fetch_send = [&](uint32_t j, uint32_t (&s)[64]) -> bool {
+        if (!wwait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sa = tmem + lane_base + kSCol + kTile * (j & 1);
+        tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld_wait();
+        // the peer has read what I sent for tile j - 1
+        if (!wwait_cluster(&bars[kXEmpty], (j & 1) ^ 1)) return false;
+        if (has_x) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            st_async_v4(x_peer + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3],
+                        xfull_peer);
+        }
         return true;
       };
       SegIter it;
@@ -578,9 +552,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t jglob = 0;
       int seg = 0;
       bool ok = true;
-      // PV #k completes phase k/2 of p_free[k % 2]; that barrier cannot run two
-      // phases ahead of this wait (its next phase needs P of tile k + 2).
-      auto wait_pv = [&](uint32_t k) -> bool { return wwait(&bars[kPFree0 + (k & 1)], (k >> 1) & 1); };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
         const int b = u / a.n_held, rs = u % a.n_held;
         const int64_t S = a.seq_lens[b];
@@ -588,20 +559,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool active = c < Rg && grow < a.R_total && S >= a.q_len;
         int64_t nvis = 0;
         if (active) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
-        // ---- query dims 0-511 of this row -> TMEM lane c, columns [256, 512)
+        // ---- this CTA's 256 c_K dims of the row -> TMEM lane c, columns [384, 512)
         if (!wwait(&bars[kQEmpty], (seg & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         {
           const bool has_row = c < Rg && grow < a.R_total;
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk);
-          for (int i = 0; i < 8; ++i) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk + 256 * (int)rank);
+#pragma unroll 1
+          for (int i = 0; i < 4; ++i) {
             uint32_t r[32];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               uint4 w4 = has_row ? __ldg(src + 8 * i + k) : make_uint4(0, 0, 0, 0);
               r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
             }
-            tmem_st32(tmem + lane_base + kQTmemCol + 32 * i, r);
+            tmem_st32(tmem + lane_base + kQCol + 32 * i, r);
           }
           tmem_st_wait();
         }
@@ -610,27 +583,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kQFull]);
         ++seg;
         float m_ref = -INFINITY, l = 0.f;
+        uint32_t s[64];  // score bits of the current tile
+        if (!fetch_send(jglob, s)) { ok = false; break; }
         for (int jj = 0; jj < nt; ++jj, ++jglob) {
-          const int sb = jglob % nsbuf;
-          if (!wwait(&bars[kSFull0 + sb], (jglob / nsbuf) & 1)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t sr[64];
-          tmem_ld32(tmem + lane_base + 2 * Rg + kTile * sb, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(tmem + lane_base + 2 * Rg + kTile * sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-          tmem_ld_wait();
-          tc_fence_before();
+          const uint32_t j = jglob;
+          // ---- the peer's partial scores of tile j: S = mine + peer's
+          if (!wwait_cluster(&bars[kXFull], j & 1)) { ok = false; break; }
+          if (has_x) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint4 w4 = x_mine[i ^ (c & 15)];
+              s[4 * i] = __float_as_uint(__uint_as_float(s[4 * i]) + __uint_as_float(w4.x));
+              s[4 * i + 1] = __float_as_uint(__uint_as_float(s[4 * i + 1]) + __uint_as_float(w4.y));
+              s[4 * i + 2] = __float_as_uint(__uint_as_float(s[4 * i + 2]) + __uint_as_float(w4.z));
+              s[4 * i + 3] = __float_as_uint(__uint_as_float(s[4 * i + 3]) + __uint_as_float(w4.w));
+            }
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
+          if (lane == 0) {
+            mbar_arrive_cluster(xempty_peer);
+            // the next phase of my receive barrier expects the peer's next tile
+            if (warp == 4 && j + 1 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
+          }
+          // ---- start the next tile's exchange before this tile's softmax
+          uint32_t s2[64];
+          if (jj + 1 < nt) {
+            if (!fetch_send(j + 1, s2)) { ok = false; break; }
+          }
+          // ---- online softmax of tile j
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
           const int64_t lim = nvis - rho0;  // columns k < lim are visible to this row
           if (lim < kTile) {
 #pragma unroll
             for (int k = 0; k < 64; ++k)
-              if (k >= lim) sr[k] = __float_as_uint(-INFINITY);
+              if (k >= lim) s[k] = __float_as_uint(-INFINITY);
           }
           float mraw = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) mraw = fmaxf(mraw, __uint_as_float(sr[k]));
+          for (int k = 0; k < 64; ++k) mraw = fmaxf(mraw, __uint_as_float(s[k]));
           const float mt = mraw * a.scale_log2;  // scale > 0: the max commutes with the scaling
           bool need = false;
           float alpha = 1.f;
@@ -641,26 +631,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             alpha = exp2f(m_ref - mt);
             m_ref = mt;
           }
-          const uint32_t abuf = (gphase & 1) * 128;
-          alpha_s[abuf + c] = alpha;
-          bool any = false;
-          if (!group_sync(need, &any)) { ok = false; break; }
-          const int pb = jglob & 1;
-          if (!wwait(&bars[kPFree0 + pb], ((jglob >> 1) & 1) ^ 1)) { ok = false; break; }
-          if (any) {
-            // O^T columns of the rows whose maximum moved are scaled by alpha
-            if (!wait_pv(jglob - 1)) { ok = false; break; }
+          if (__any_sync(0xffffffffu, need)) {
+            // rows whose maximum moved: scale their O row once PV(j - 1) is done
+            // (a row's maximum is finite only after a tile of this segment, so j >= 1)
+            if (!wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
-            for (int t = 0; t < 2; ++t) {
-              for (int c0 = 0; c0 < Rg; c0 += 16) {
-                uint32_t r[16];
-                const uint32_t addr = tmem + lane_base + t * Rg + c0;
-                tmem_ld16(addr, r);
-                tmem_ld_wait();
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {
+              uint32_t r[32];
+              const uint32_t addr = tmem + lane_base + kOCol + 32 * q;
+              tmem_ld32(addr, r);
+              tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[abuf + c0 + i]);
-                tmem_st16(addr, r);
-              }
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(addr, r);
             }
             tmem_st_wait();
             l *= alpha;
@@ -668,71 +652,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           const float cs = a.scale_log2;
           float psum = 0.f;
-          uint32_t pk[32];
+          // P over the first 32 columns of the tile's S (A operand of the PV product)
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * k]), cs, -m_use));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * k + 1]), cs, -m_use));
-            psum += p0 + p1;
-            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            pk[k] = *reinterpret_cast<uint32_t*>(&h);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int e = 32 * h2 + 2 * k;
+              const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cs, -m_use));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cs, -m_use));
+              psum += p0 + p1;
+              __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+              pk[k] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            tmem_st16(tmem + lane_base + kSCol + kTile * (j & 1) + 16 * h2, pk);
           }
           l += psum;
-          if (c < Rg) {
-            // row c of the K-major, 128B-swizzled P tile: 8 x 16-byte pieces
-            unsigned char* row = p_s + pb * Rg * 128 + (c >> 3) * 1024 + (c & 7) * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint4 w4 = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-              *reinterpret_cast<uint4*>(row + ((q ^ (c & 7)) << 4)) = w4;
-            }
-          }
-          fence_proxy_async_smem();
+          tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kPFull0 + pb]);
+          if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
+#pragma unroll
+          for (int k = 0; k < 64; ++k) s[k] = s2[k];
         }
         if (!ok) break;
-        // ---------------- epilogue: O^T (my dims x rows) / l -> o, lse
-        if (!wait_pv(jglob - 1)) { ok = false; break; }
+        // ---------------- epilogue: O row / l -> o (this CTA's 256 dims), lse
+        const uint32_t jl = jglob - 1;
+        if (!wwait(&bars[kPVDone0 + (jl & 1)], (jl >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const uint32_t ibuf = (gphase & 1) * 128;
-        inv_s[ibuf + c] = inv;
         const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-        bool dummy;
-        if (!group_sync(false, &dummy)) { ok = false; break; }
         const int R_here = min(Rg, a.R_total - g * Rg);
-        const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total + g * Rg;
-        const int64_t piece = (int64_t)(2 * v + kslot) * a.R_total + g * Rg;
-        for (int t = 0; t < 2; ++t) {
-          for (int c0 = 0; c0 < Rg; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(tmem + lane_base + t * Rg + c0, r);
-            tmem_ld_wait();
-            const int dim = 256 * (int)rank + t * 128 + c;
+        const bool writes = c < R_here;
+        const int64_t out_row = ((int64_t)rs * a.B + b) * a.R_total + g * Rg + c;
+        const int64_t piece_row = (int64_t)(2 * v + kslot) * a.R_total + g * Rg + c;
+#pragma unroll 1
+        for (int q = 0; q < 8; ++q) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + kOCol + 32 * q, r);
+          tmem_ld_wait();
+          if (writes) {
+            const int d0 = 256 * (int)rank + 32 * q;
+            if (whole && a.o_bf16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d0);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int row = c0 + i;
-              if (row < R_here) {
-                const float val = __uint_as_float(r[i]) * inv_s[ibuf + row];
-                if (whole) {
-                  if (a.o_bf16)
-                    static_cast<__nv_bfloat16*>(a.o_part)[(out_row0 + row) * kDv + dim] = __float2bfloat16_rn(val);
-                  else
-                    static_cast<float*>(a.o_part)[(out_row0 + row) * kDv + dim] = val;
-                } else {
-                  a.piece_o[(piece + row) * kDv + dim] = val;
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
+                                                           __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
+                  w[e] = *reinterpret_cast<uint32_t*>(&h);
                 }
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
               }
+            } else {
+              float* base = whole ? static_cast<float*>(a.o_part) + out_row * kDv + d0 : a.piece_o + piece_row * kDv + d0;
+              float4* dst = reinterpret_cast<float4*>(base);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                     __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
             }
           }
         }
-        if (c < R_here && rank == 0) {
+        if (writes && rank == 0) {
           if (whole)
-            a.lse_part[out_row0 + c] = a.base2 ? lse2 : lse2 * kLn2;
+            a.lse_part[out_row] = a.base2 ? lse2 : lse2 * kLn2;
           else
-            a.piece_lse[piece + c] = lse2;
+            a.piece_lse[piece_row] = lse2;
         }
         tc_fence_before();
         __syncwarp();
@@ -744,7 +732,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (*abort_s && tid == 0) flag(a.status, DCP_STATUS_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  // The peer may still have copies or arrivals addressed to this CTA's shared
+  // The peer may still have stores or arrivals addressed to this CTA's shared
   // memory; retire the pair together.  After an abort, allow in-flight tensor
   // core commits (microseconds) to land first.
   if (*abort_s) __nanosleep(100000);
@@ -825,7 +813,7 @@ __global__ void __launch_bounds__(256) fixup_kernel(TcArgs a) {
 
 // ---------------------------------------------------------------------------- host side
 struct Plan {
-  int Rg, ngroups, V, nslot, nsbuf, box_rows;
+  int Rg, ngroups, V, nts, box_rows;
   size_t smem;
   size_t ws_start_bytes, ws_piece_o_bytes, ws_piece_lse_bytes, ws_total;
 };
@@ -874,12 +862,10 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   if (p->V < 1) p->V = 1;
   const SmemLayout base = smem_layout(p->Rg, 0);
   const size_t budget = 232448 - 1024;  // 227 KB minus alignment slack
-  int nslot = (int)((budget - base.total) / kChunkBytes);
-  nslot &= ~1;
-  if (nslot > kMaxSlots) nslot = kMaxSlots;
-  p->nslot = nslot;
-  p->nsbuf = (2 * p->Rg + 2 * kTile <= kQTmemCol) ? 2 : 1;
-  p->smem = smem_layout(p->Rg, nslot).total + 1024;
+  int nts = (int)((budget - base.total) / (kSlotBytes + kChunkBytes));
+  if (nts > kMaxTileSlots) nts = kMaxTileSlots;
+  p->nts = nts;
+  p->smem = smem_layout(p->Rg, nts).total + 1024;
   // clusters that can be resident at once (both CTAs of a cluster share a GPC)
   const int clusters = max_active_clusters(p->smem);
   if (clusters > 0) {
@@ -893,7 +879,7 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   p->ws_piece_o_bytes = align256((size_t)2 * p->V * R_total * kDv * 4);
   p->ws_piece_lse_bytes = align256((size_t)2 * p->V * R_total * 4);
   p->ws_total = p->ws_start_bytes + p->ws_piece_o_bytes + p->ws_piece_lse_bytes;
-  return nslot >= 2 * kKSlots;
+  return nts >= 3;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -984,7 +970,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   a.shard_begin = shard_begin;
   a.n_held = n_held;
   a.B = B; a.q_len = q_len; a.H = H; a.R_total = q_len * H;
-  a.Rg = p.Rg; a.ngroups = p.ngroups; a.V = p.V; a.nslot = p.nslot; a.nsbuf = p.nsbuf; a.box_rows = p.box_rows;
+  a.Rg = p.Rg; a.ngroups = p.ngroups; a.V = p.V; a.nts = p.nts; a.box_rows = p.box_rows;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.pool_rows = pool_rows; a.pool_pages = pool_pages;
   a.bt = block_table; a.bt_stride = bt_stride; a.max_pages = max_pages;
