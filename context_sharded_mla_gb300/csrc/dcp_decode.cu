@@ -57,13 +57,18 @@ constexpr int kTile = 64;                     // KV rows per tile
 constexpr int kChunkDims = 64;                // dims per chunk (one 128-byte swizzle row)
 constexpr int kChunkBytes = kTile * 128;      // 8 KB
 constexpr int kOwnChunks = 4;                 // value chunks each CTA loads (256 dims)
-constexpr int kSlotBytes = kOwnChunks * kChunkBytes;
+constexpr int kRopeHalf = 32;                 // rope dims each CTA loads (64-byte swizzled rows)
+constexpr int kRopeHalfBytes = kTile * 64;
+constexpr int kRopeOff = kOwnChunks * kChunkBytes;         // rope part inside a tile slot
+constexpr int kSlotBytes = kRopeOff + kRopeHalfBytes;      // 36 KB per tile slot
 constexpr int kMaxTileSlots = 8;
-constexpr int kThreads = 192;                 // 6 warps: producer, MMA issuer, 4 softmax/epilogue
+constexpr int kThreads = 320;                 // 10 warps: producer, MMA issuer, 4 softmax/epilogue, 4 senders
 constexpr int kMaxGroupRows = 128;
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
-constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns (P over them)
-constexpr uint32_t kQCol = 384;               // [384, 512): the query's c_K half as bf16 pairs
+constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns
+constexpr uint32_t kPCol = 384;               // [384, 416): P of one tile as bf16 pairs
+constexpr uint32_t kQCol = 416;               // [416, 512): query chunks 4r .. 4r + 2 as bf16 pairs
+constexpr int kQTmemChunks = 3;               // query chunk 4r + 3 is read from shared memory
 constexpr int kXRowBytes = kTile * 4;         // one row of a partial score tile (fp32)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -93,25 +98,28 @@ struct TcArgs {
 };
 
 struct SmemLayout {
-  uint32_t qr, x, ring, rope, bars, misc, total;
+  uint32_t qc, qr, x, xbuf, ring, rope, bars, misc, total;
 };
 
 __host__ __device__ inline uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   SmemLayout s;
-  s.qr = 0;                                        // rope dims of the query rows: [128][64] bf16, swizzled
-  s.x = 128 * 128;                                 // the peer's partial scores: [Rg][64] fp32
-  s.ring = s.x + round1024((uint32_t)Rg * kXRowBytes);
-  s.rope = s.ring + nts * kSlotBytes;              // rope chunk of each tile slot (CTA 0)
-  s.bars = s.rope + nts * kChunkBytes;
+  s.qc = 0;                                        // query chunk 4r + 3: [128][64] bf16, 128-byte swizzle
+  s.qr = 128 * 128;                                // query rope dims [32r, 32r + 32): [128][32], 64-byte swizzle
+  s.x = s.qr + 128 * 64;                           // the peer's partial scores, two buffers of [Rg][64] fp32
+  s.xbuf = round1024((uint32_t)Rg * kXRowBytes);
+  s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
+  s.rope = s.ring;                                 // (kept for the layout struct; rope lives in the slots)
+  s.bars = s.ring + nts * kSlotBytes;
   s.misc = s.bars + (16 + 2 * kMaxTileSlots) * 8;
   s.total = s.misc + 64;
   return s;
 }
 
-enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree, kXFull, kXEmpty,
-           kNumFixedBars };
+enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
+           kXFull0, kXFull1, kXEmpty0, kXEmpty1, kNumFixedBars };
+static_assert(kNumFixedBars <= 16, "fixed barriers");
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
   const int64_t S = a.seq_lens[b];
@@ -215,23 +223,44 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Warp-uniform bounded waits: lane 0 polls and broadcasts; on success every lane
+// tests the completed phase once more, which gives each lane its own acquire.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_s, int lane) {
+  int r = 1;
+  if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
+  r = __shfl_sync(0xffffffffu, r, 0);
+  if (r) mbar_try_wait(bar, parity);
+  return r != 0;
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_s, int lane) {
+  int r = 1;
+  if (lane == 0) r = mbar_wait_cluster(bar, parity, abort_s) ? 1 : 0;
+  r = __shfl_sync(0xffffffffu, r, 0);
+  if (r) mbar_try_wait_cluster(bar, parity);
+  return r != 0;
+}
+
 // ---------------------------------------------------------------------------- main kernel
 // A 2-CTA cluster per (work range, row group).  CTA `rank` loads key/value dims
 // [256 rank, 256 rank + 256) of every tile (CTA 0 also the 64 rope dims),
 // computes its partial scores over them, swaps partial scores with its peer and
 // accumulates its own 256 value dims of O.  Both CTAs walk the same tile
-// sequence in lockstep through the score exchange.
+// sequence; the score exchange is double-buffered and S tiles are released as
+// soon as they have been read, so QK products run up to two tiles ahead of the
+// softmax while the exchange is in flight.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
+                      const __grid_constant__ CUtensorMap tmap_q64, const __grid_constant__ CUtensorMap tmap_kv64,
                       TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemLayout sl = smem_layout(a.Rg, a.nts);
+  unsigned char* qc_s = smem + sl.qc;
   unsigned char* qr_s = smem + sl.qr;
   unsigned char* x_s = smem + sl.x;
   unsigned char* ring = smem + sl.ring;
-  unsigned char* rope = smem + sl.rope;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
   uint64_t* tfull = bars + 16;                  // tile slot landed
   uint64_t* tempty = tfull + kMaxTileSlots;     // tile slot released by its PV product
@@ -256,23 +285,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     *abort_s = 0;
     for (int i = 0; i < kNumFixedBars; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&bars[kQFull], nact + (rank == 0 ? 1 : 0));  // softmax warps (+ the rope TMA on CTA 0)
+    mbar_init(&bars[kQFull], nact + 1);  // softmax warps + the query-chunk TMA
+    mbar_init(&bars[kSFree0], 2 * nact);  // sender and softmax warps have read the partial scores
+    mbar_init(&bars[kSFree1], 2 * nact);
     mbar_init(&bars[kPFull0], nact);
     mbar_init(&bars[kPFull1], nact);
     mbar_init(&bars[kOFree], nact);
-    mbar_init(&bars[kXEmpty], nact);  // remote arrivals: the peer's warps have read my scores
+    mbar_init(&bars[kXEmpty0], nact);  // remote arrivals: the peer's warps have read my scores
+    mbar_init(&bars[kXEmpty1], nact);
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 1);
     }
     fence_barrier_init();
-    // the peer's first partial tile is expected before it can be sent
-    if (ntiles_cta > 0) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
+    // the peer's first two partial tiles are expected before they can be sent
+    for (uint32_t j = 0; j < 2 && j < ntiles_cta; ++j)
+      mbar_arrive_expect_tx(&bars[kXFull0 + j], (uint32_t)Rg * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
-  for (int i = tid; i < nts * (kSlotBytes + kChunkBytes) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < 128 * 128 / 16; i += kThreads) reinterpret_cast<uint4*>(qr_s)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  // query rows past the group are read by the M = 128 products: zeros
+  for (int i = tid; i < (128 * 128 + 128 * 64) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qc_s)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_base_s, 512);
@@ -285,9 +319,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0 && lo < hi) {
-      if (rank == 0) prefetch_tmap(&tmap_q);
-      prefetch_tmap(&tmap_kv);
+    // The whole warp walks the tile sequence: its lanes fetch the block-table
+    // entries of 32 tiles at a time (the next 32 are already in flight), lane 0
+    // takes each tile's page ids by shuffle, waits for the ring slot and issues
+    // the TMA copies.  Waits are lane-0 polls broadcast to the warp.
+    if (lo < hi) {
+      if (lane == 0) {
+        prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_kv);
+        prefetch_tmap(&tmap_q64);
+        prefetch_tmap(&tmap_kv64);
+      }
       SegIter it;
       it.init(a.tile_start, U, lo, hi);
       int32_t u, t0, nt, kslot;
@@ -307,14 +349,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (q == i) y = bx.y[i];
         return y;
       };
-      // page ids are fetched one tile ahead (raw loads consumed a tile later)
-      auto fetch_pages = [&](int b, int64_t nvis, int32_t tile, int32_t (&pg)[8]) {
+      // lane l: page ids of the boxes of tile tile0 + l (-2: not needed, -1: past the table)
+      auto fetch_batch = [&](int b, int64_t nvis, int32_t tile0, int32_t tile_end, int32_t (&pg)[8]) {
+        const int32_t tile = tile0 + lane;
         const int64_t rho0 = (int64_t)tile * kTile;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          pg[q] = -2;  // not needed
+          pg[q] = -2;
           const int64_t rho = rho0 + (int64_t)q * a.box_rows;
-          if (q < nbox && rho < nvis) {
+          if (tile < tile_end && q < nbox && rho < nvis) {
             const int64_t pidx = rho / a.L.P;
             pg[q] = pidx < a.max_pages ? __ldg(a.bt + (int64_t)b * a.bt_stride + pidx) : -1;
           }
@@ -328,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bx.y[q] = -1;
           if (pg[q] == -2) continue;
           if (pg[q] < 0 || pg[q] >= a.pool_pages) {
-            if (rank == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+            if (rank == 0 && lane == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
             continue;
           }
           const int64_t rho = rho0 + (int64_t)q * a.box_rows;
@@ -348,36 +391,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       };
-      const int nchunks = rank == 0 ? kOwnChunks + 1 : kOwnChunks;
+      // this CTA's 32 rope dims of the tile: rows of 64 bytes, 64-byte swizzle
+      auto issue_rope = [&](const Boxes& bx, unsigned char* dst, uint64_t* bar) {
+        const int32_t x = 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank;
+        if (nbox == 1) {
+          if (bx.y[0] >= 0) tma_load_2d(dst, &tmap_kv64, bar, x, bx.y[0]);
+        } else {
+          for (int q = 0; q < nbox; ++q) {
+            const int32_t y = box_y(bx, q);
+            if (y >= 0) tma_load_2d(dst + q * a.box_rows * 64, &tmap_kv64, bar, x, y);
+          }
+        }
+      };
+      uint32_t ts = 0, tphase = 0;  // ring slot of tile j and its use parity
       auto load_tile = [&](const Boxes& bx) -> bool {
-        const uint32_t ts = j % nts;
-        if (!mbar_wait(&tempty[ts], ((j / nts) & 1) ^ 1, abort_s)) return false;
-        mbar_arrive_expect_tx(&tfull[ts], bx.bytes * nchunks);
-        unsigned char* dst = ring + ts * kSlotBytes;
-        for (int i = 0; i < kOwnChunks; ++i)
-          issue_chunk(bx, dst + i * kChunkBytes, &tfull[ts], kOwnChunks * (int)rank + i);
-        if (rank == 0) issue_chunk(bx, rope + ts * kChunkBytes, &tfull[ts], 2 * kOwnChunks);
+        if (!warp_wait(&tempty[ts], tphase ^ 1, abort_s, lane)) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&tfull[ts], bx.bytes * kOwnChunks + bx.bytes / 2);
+          unsigned char* dst = ring + ts * kSlotBytes;
+          for (int i = 0; i < kOwnChunks; ++i)
+            issue_chunk(bx, dst + i * kChunkBytes, &tfull[ts], kOwnChunks * (int)rank + i);
+          issue_rope(bx, dst + kRopeOff, &tfull[ts]);
+        }
         ++j;
+        if (++ts == (uint32_t)nts) {
+          ts = 0;
+          tphase ^= 1;
+        }
         return true;
       };
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
         const int b = u / a.n_held, rs = u % a.n_held;
         bool bad = false;
         const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
-        int32_t pg_next[8];
-        fetch_pages(b, nvis, t0, pg_next);
-        if (rank == 0) {
-          if (!mbar_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars[kQFull], Rg * 128);
-          tma_load_2d(qr_s, &tmap_q, &bars[kQFull], 2 * kOwnChunks * kChunkDims, b * a.R_total + g * Rg);
+        const int32_t t_end = t0 + nt;
+        int32_t pgc[8], pgn[8];
+        fetch_batch(b, nvis, t0, t_end, pgc);
+        fetch_batch(b, nvis, t0 + 32, t_end, pgn);
+        // the query's chunk 4r + 3 and its rope dims [32r, 32r + 32) for the SS part of QK
+        if (!warp_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s, lane)) { ok = false; break; }
+        if (lane == 0) {
+          const int32_t qy = b * a.R_total + g * Rg;
+          mbar_arrive_expect_tx(&bars[kQFull], Rg * (128 + 64));
+          tma_load_2d(qc_s, &tmap_q, &bars[kQFull], (kOwnChunks * (int)rank + kQTmemChunks) * kChunkDims, qy);
+          tma_load_2d(qr_s, &tmap_q64, &bars[kQFull], 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, qy);
         }
         ++seg;
-        Boxes cur;
-        make_boxes(rs, t0, pg_next, cur);
         for (int jj = 0; jj < nt && ok; ++jj) {
-          if (jj + 1 < nt) fetch_pages(b, nvis, t0 + jj + 1, pg_next);
+          if (jj > 0 && (jj & 31) == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pgc[q] = pgn[q];
+            fetch_batch(b, nvis, t0 + jj + 32, t_end, pgn);
+          }
+          int32_t pg[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xffffffffu, pgc[q], jj & 31);
+          Boxes cur;
+          make_boxes(rs, t0 + jj, pg, cur);
           ok = load_tile(cur);
-          if (jj + 1 < nt) make_boxes(rs, t0 + jj + 1, pg_next, cur);
         }
       }
       // Drain: every slot's last release (a tensor-core commit) lands before the
@@ -385,42 +456,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (ok) {
         for (uint32_t s = 0; s < (uint32_t)nts && s < ntiles_cta; ++s) {
           const uint32_t last = s + ((ntiles_cta - 1 - s) / nts) * nts;  // last tile in slot s
-          if (!mbar_wait(&tempty[s], (last / nts) & 1, abort_s)) break;
+          if (!warp_wait(&tempty[s], (last / nts) & 1, abort_s, lane)) break;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Event-driven single thread.  Tensor-core operations issued by one thread
-    // run in issue order, so QK(j + 2) may be issued right after PV(j): it
-    // overwrites the S/P tile that PV(j) reads only after PV(j) has read it.
+    // Event-driven single thread: QK(j) once tile j has landed and the S tile it
+    // writes (last used by tile j - 2) has been read; PV(j) once P(j) is ready.
     if (lane == 0 && lo < hi) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t kdesc0 = sw128_desc(smem_u32(ring), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
-      const uint64_t qrdesc0 = sw128_desc(smem_u32(qr_s), 16, 1024);
-      const uint64_t rdesc0 = sw128_desc(smem_u32(rope), 16, 1024);
-      auto issue_qk = [&](uint32_t j) {
-        const uint32_t ts = j % nts;
+      const uint64_t qcdesc0 = sw128_desc(smem_u32(qc_s), 16, 1024);
+      const uint64_t qrdesc0 = sw64_desc(smem_u32(qr_s), 512);
+      const uint64_t rdesc0 = sw64_desc(smem_u32(ring + kRopeOff), 512);
+      // QK(j): query chunks 4r .. 4r + 2 from TMEM (12 MMAs), chunk 4r + 3 and the
+      // rope half from shared memory (4 + 2 MMAs), back to back.  (Issuing the
+      // product in pieces with PV products slipped in between was measured
+      // slower: it delays the scores that the exchange is waiting for.)
+      auto issue_qk = [&](uint32_t j, uint32_t ts) {
         const uint32_t d = tmem + kSCol + kTile * (j & 1);
+        const uint32_t soff = (ts * kSlotBytes) >> 4;
+        const uint64_t kd = kdesc0 + soff;
 #pragma unroll
-        for (int i = 0; i < kOwnChunks; ++i) {
-          const uint64_t kd = kdesc0 + ((ts * kSlotBytes + i * kChunkBytes) >> 4);
+        for (int i = 0; i < kQTmemChunks; ++i)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(d, tmem + kQCol + 32 * i + 8 * kk, kd + 2 * kk, idesc_qk, (i | kk) != 0);
-        }
-        if (rank == 0) {
-          const uint64_t rd = rdesc0 + ((ts * kChunkBytes) >> 4);
+            mma_bf16_ts(d, tmem + kQCol + 32 * i + 8 * kk, kd + i * (kChunkBytes >> 4) + 2 * kk, idesc_qk,
+                        (i | kk) != 0);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rd + 2 * kk, idesc_qk, 1);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(d, qcdesc0 + 2 * kk, kd + kQTmemChunks * (kChunkBytes >> 4) + 2 * kk, idesc_qk, 1);
+#pragma unroll
+        for (int kk = 0; kk < kRopeHalf / 16; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rdesc0 + soff + 2 * kk, idesc_qk, 1);
         mma_commit(&bars[kSFull0 + (j & 1)]);
       };
-      auto issue_pv = [&](uint32_t j, bool first) {
-        const uint32_t ts = j % nts;
-        const uint32_t pa = tmem + kSCol + kTile * (j & 1);  // P: 64 bf16 = 32 columns
+      auto issue_pv = [&](uint32_t j, uint32_t ts, bool first) {
+        const uint32_t pa = tmem + kPCol;  // P: 64 bf16 = 32 columns
         const uint64_t vd = vdesc0 + ((ts * kSlotBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -428,6 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mma_commit(&tempty[ts]);
         mma_commit(&bars[kPVDone0 + (j & 1)]);
       };
+      uint32_t ts_q = 0, ph_q = 0, ts_p = 0;  // ring slots of the next QK and PV products
       SegIter itq;
       itq.init(a.tile_start, U, lo, hi);
       int32_t uq, t0q, ntq, ksq;
@@ -452,7 +527,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ready && p_jj == 0 && p_seg >= 1) ready = mbar_test(&bars[kOFree], (p_seg - 1) & 1);
           if (ready) {
             tc_fence_after();
-            issue_pv(jp, p_jj == 0);
+            issue_pv(jp, ts_p, p_jj == 0);
+            if (++ts_p == (uint32_t)nts) ts_p = 0;
             ++jp;
             if (++p_jj == ntp) {
               ++p_seg;
@@ -462,14 +538,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progress = true;
           }
         }
-        if (q_has && jq <= jp + 1) {  // the S/P tile of jq was last read by PV(jq - 2)
-          if (!q_seg_ready && mbar_test(&bars[kQFull], q_seg & 1)) {
-            q_seg_ready = true;
-            progress = true;
-          }
-          if (q_seg_ready && mbar_test(&tfull[jq % nts], (jq / nts) & 1)) {
+        // the S tile of jq was last used by tile jq - 2: both its readers must be
+        // done before QK(jq) starts; the whole product goes out back to back
+        if (q_has && mbar_test(&bars[kSFree0 + (jq & 1)], ((jq >> 1) & 1) ^ 1)) {
+          if (!q_seg_ready && mbar_test(&bars[kQFull], q_seg & 1)) q_seg_ready = true;
+          if (q_seg_ready && mbar_test(&tfull[ts_q], ph_q)) {
             tc_fence_after();
-            issue_qk(jq);
+            issue_qk(jq, ts_q);
+            if (++ts_q == (uint32_t)nts) {
+              ts_q = 0;
+              ph_q ^= 1;
+            }
             if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
             ++jq;
             if (++q_jj == ntq) {
@@ -496,54 +575,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (32 * (warp & 3) < Rg) {
-    // ------------------------------------------------------------------ Q load, score exchange, softmax, epilogue
-    // Waits are polled by one lane per warp and broadcast, so a timeout drains
-    // every thread.  A thread owns query row c (TMEM lane c) of the group.
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------------ score senders
+    // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32): each tile's partial scores
+    // go to the peer's exchange buffer (16-byte pieces, 256-byte rows swizzled by
+    // row so a warp's stores spread over all banks), off the softmax warps' path.
     const int c = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const bool has_x = c < Rg;  // this row's partial scores cross to the peer
-    const uint32_t peer = rank ^ 1u;
-    const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer) + (uint32_t)c * kXRowBytes;
-    const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull]), peer);
-    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty]), peer);
-    const uint4* x_mine = reinterpret_cast<const uint4*>(x_s + c * kXRowBytes);
-    if (lo < hi) {
-      // Lane 0 polls (bounded) and broadcasts; on success every lane tests the
-      // completed phase once more, which gives each lane its own acquire.
-      auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        int r = 1;
-        if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
-        r = __shfl_sync(0xffffffffu, r, 0);
-        if (r) mbar_try_wait(bar, parity);
-        return r != 0;
-      };
-      auto wwait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
-        int r = 1;
-        if (lane == 0) r = mbar_wait_cluster(bar, parity, abort_s) ? 1 : 0;
-        r = __shfl_sync(0xffffffffu, r, 0);
-        if (r) mbar_try_wait_cluster(bar, parity);
-        return r != 0;
-      };
-      // Scores of tile j: read this CTA's partial from TMEM and send it to the
-      // peer (16-byte pieces, 128-byte rows swizzled by row so a warp's stores
-      // spread over all banks).
-      auto fetch_send = [&](uint32_t j, uint32_t (&s)[64]) -> bool {
-        if (!wwait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) return false;
+    if (32 * (warp & 3) < Rg && lo < hi) {
+      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+      const bool has_x = c < Rg;
+      const uint32_t peer = rank ^ 1u;
+      const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer) + (uint32_t)c * kXRowBytes;
+      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull0]), peer);
+      for (uint32_t j = 0; j < ntiles_cta; ++j) {
+        uint32_t s[64];
+        if (!warp_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_s, lane)) break;
         tc_fence_after();
         const uint32_t sa = tmem + lane_base + kSCol + kTile * (j & 1);
         tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_ld_wait();
-        // the peer has read what I sent for tile j - 1
-        if (!wwait_cluster(&bars[kXEmpty], (j & 1) ^ 1)) return false;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
+        // the peer has read what was sent for tile j - 2 (two exchange buffers)
+        const uint32_t xb = j & 1;
+        if (!warp_wait_cluster(&bars[kXEmpty0 + xb], ((j >> 1) & 1) ^ 1, abort_s, lane)) break;
         if (has_x) {
+          const uint32_t dst = x_peer + xb * sl.xbuf;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            st_async_v4(x_peer + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3],
-                        xfull_peer);
+            st_async_v4(dst + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3],
+                        xfull_peer + 8 * xb);
         }
-        return true;
+      }
+    }
+  } else if (32 * (warp & 3) < Rg) {
+    // ------------------------------------------------------------------ Q load, softmax, epilogue
+    // Waits are polled by one lane per warp and broadcast, so a timeout drains
+    // every thread.  A thread owns query row c (TMEM lane c) of the group.
+    const int c = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const bool has_x = c < Rg;  // this row's partial scores cross between the CTAs
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty0]), peer);
+    const uint32_t x_mine = smem_u32(x_s) + (uint32_t)c * kXRowBytes;
+    if (lo < hi) {
+      auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_s, lane); };
+      auto wwait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return warp_wait_cluster(bar, parity, abort_s, lane);
       };
       SegIter it;
       it.init(a.tile_start, U, lo, hi);
@@ -559,7 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool active = c < Rg && grow < a.R_total && S >= a.q_len;
         int64_t nvis = 0;
         if (active) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
-        // ---- this CTA's 256 c_K dims of the row -> TMEM lane c, columns [384, 512)
+        // ---- this CTA's first 192 c_K dims of the row -> TMEM lane c, columns [416, 512)
         if (!wwait(&bars[kQEmpty], (seg & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         {
@@ -567,7 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint4* src =
               reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk + 256 * (int)rank);
 #pragma unroll 1
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < kQTmemChunks; ++i) {
             uint32_t r[32];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -583,32 +663,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kQFull]);
         ++seg;
         float m_ref = -INFINITY, l = 0.f;
-        uint32_t s[64];  // score bits of the current tile
-        if (!fetch_send(jglob, s)) { ok = false; break; }
         for (int jj = 0; jj < nt; ++jj, ++jglob) {
           const uint32_t j = jglob;
+          // ---- this CTA's partial scores of tile j
+          uint32_t s[64];  // score bits
+          if (!wwait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint32_t sa = tmem + lane_base + kSCol + kTile * (j & 1);
+            tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            tmem_ld_wait();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
           // ---- the peer's partial scores of tile j: S = mine + peer's
-          if (!wwait_cluster(&bars[kXFull], j & 1)) { ok = false; break; }
+          const uint32_t xb = j & 1;
+          if (!wwait_cluster(&bars[kXFull0 + xb], (j >> 1) & 1)) { ok = false; break; }
           if (has_x) {
+            const uint32_t src = x_mine + xb * sl.xbuf;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint4 w4 = x_mine[i ^ (c & 15)];
+              const uint4 w4 = ld_shared_v4(src + ((uint32_t)(i ^ (c & 15)) << 4));
               s[4 * i] = __float_as_uint(__uint_as_float(s[4 * i]) + __uint_as_float(w4.x));
               s[4 * i + 1] = __float_as_uint(__uint_as_float(s[4 * i + 1]) + __uint_as_float(w4.y));
               s[4 * i + 2] = __float_as_uint(__uint_as_float(s[4 * i + 2]) + __uint_as_float(w4.z));
               s[4 * i + 3] = __float_as_uint(__uint_as_float(s[4 * i + 3]) + __uint_as_float(w4.w));
             }
           }
+          // The adds above consumed every lane's reads, so the buffer is free once
+          // the warp has passed this point; the release to the peer needs no fence.
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_cluster(xempty_peer);
-            // the next phase of my receive barrier expects the peer's next tile
-            if (warp == 4 && j + 1 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
-          }
-          // ---- start the next tile's exchange before this tile's softmax
-          uint32_t s2[64];
-          if (jj + 1 < nt) {
-            if (!fetch_send(j + 1, s2)) { ok = false; break; }
+            mbar_arrive_cluster_relaxed(xempty_peer + 8 * xb);
+            // the next phase of this receive buffer expects the peer's tile j + 2
+            if (warp == 4 && j + 2 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull0 + xb], (uint32_t)Rg * kXRowBytes);
           }
           // ---- online softmax of tile j
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
@@ -618,9 +708,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 64; ++k)
               if (k >= lim) s[k] = __float_as_uint(-INFINITY);
           }
-          float mraw = -INFINITY;
+          float mx[8];
 #pragma unroll
-          for (int k = 0; k < 64; ++k) mraw = fmaxf(mraw, __uint_as_float(s[k]));
+          for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(s[k]);
+#pragma unroll
+          for (int k = 8; k < 64; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(s[k]));
+          const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
           const float mt = mraw * a.scale_log2;  // scale > 0: the max commutes with the scaling
           bool need = false;
           float alpha = 1.f;
@@ -631,10 +725,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             alpha = exp2f(m_ref - mt);
             m_ref = mt;
           }
+          // PV(j - 1) must be done before O is rescaled or P is overwritten
+          bool pv_prev_done = j == 0;
           if (__any_sync(0xffffffffu, need)) {
-            // rows whose maximum moved: scale their O row once PV(j - 1) is done
+            // rows whose maximum moved: scale their O row
             // (a row's maximum is finite only after a tile of this segment, so j >= 1)
             if (!wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
+            pv_prev_done = true;
             tc_fence_after();
 #pragma unroll 1
             for (int q = 0; q < 8; ++q) {
@@ -651,29 +748,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           const float cs = a.scale_log2;
-          float psum = 0.f;
-          // P over the first 32 columns of the tile's S (A operand of the PV product)
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[32];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int e = 32 * h2 + 2 * k;
-              const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cs, -m_use));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cs, -m_use));
-              psum += p0 + p1;
-              __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-              pk[k] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            tmem_st16(tmem + lane_base + kSCol + kTile * (j & 1) + 16 * h2, pk);
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[2 * k]), cs, -m_use));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[2 * k + 1]), cs, -m_use));
+            ps[k & 3] += p0 + p1;
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&h);
           }
-          l += psum;
+          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          // P -> TMEM (A operand of the PV product) once PV(j - 1) has read the previous P
+          if (!pv_prev_done && !wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          tmem_st32(tmem + lane_base + kPCol, pk);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
-#pragma unroll
-          for (int k = 0; k < 64; ++k) s[k] = s2[k];
         }
         if (!ok) break;
         // ---------------- epilogue: O row / l -> o (this CTA's 256 dims), lse
@@ -862,7 +955,7 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   if (p->V < 1) p->V = 1;
   const SmemLayout base = smem_layout(p->Rg, 0);
   const size_t budget = 232448 - 1024;  // 227 KB minus alignment slack
-  int nts = (int)((budget - base.total) / (kSlotBytes + kChunkBytes));
+  int nts = (int)((budget - base.total) / kSlotBytes);
   if (nts > kMaxTileSlots) nts = kMaxTileSlots;
   p->nts = nts;
   p->smem = smem_layout(p->Rg, nts).total + 1024;
@@ -896,17 +989,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [rows, 576] row-major, 128-byte swizzled boxes of [box_rows, 64]
-bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// bf16 [rows, 576] row-major, boxes of [box_rows, 64] with 128-byte swizzle, or
+// (half = true) boxes of [box_rows, 32] with 64-byte swizzle
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool half = false) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kChunkDims, box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)(half ? kRopeHalf : kChunkDims), box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, half ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool page_size_ok(int P) { return P >= 8 && P % 8 == 0 && (P % kTile == 0 || kTile % P == 0); }
@@ -953,9 +1047,11 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   if (!workspace || workspace_bytes < p.ws_total) return DCP_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return DCP_ERR_INVALID;
 
-  CUtensorMap tq, tkv;
+  CUtensorMap tq, tkv, tq64, tkv64;
   if (!make_tmap(&tq, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg)) return DCP_ERR_CUDA;
   if (!make_tmap(&tkv, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
+  if (!make_tmap(&tq64, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg, true)) return DCP_ERR_CUDA;
+  if (!make_tmap(&tkv64, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows, true)) return DCP_ERR_CUDA;
 
   static size_t smem_set = 0;
   if (smem_set < p.smem) {
@@ -986,7 +1082,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   cudaStream_t st = as_stream(stream);
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
-  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, a);
+  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, a);
   fixup_kernel<<<U, 256, 0, st>>>(a);
   return launch_status(3);
 }

@@ -257,6 +257,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr)
+               : "memory");
+  return v;
+}
+
 // 16 bytes from registers into another CTA's shared memory (`cluster_addr`,
 // from mapa); the mbarrier at `cluster_bar` in that CTA is credited with the
 // 16 bytes when they have landed (complete_tx), so the receiver needs no fence.
@@ -266,6 +273,14 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, u
                    cluster_addr),
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
                : "memory");
+}
+
+// Arrive without release semantics on an mbarrier that may live in another CTA.
+// For signalling "I have read your data" after the reads' values were consumed:
+// a release arrive at cluster scope waits (about a microsecond) for this
+// thread's earlier memory operations, which such a signal does not need.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA 2-D load written to the same offset in every CTA of `cta_mask`; each
@@ -299,6 +314,13 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Same, 64-byte swizzle (layout code 4): K-major rows of 32 bf16 = 64 B, 8-row
+// atoms of 512 B (SBO = 512); advance K by 16 elements with start += 32 B.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1u) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an f32 accumulator.
