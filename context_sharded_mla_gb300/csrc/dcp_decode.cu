@@ -9,31 +9,36 @@
 // "DCP x speculative decoding" (causal mask in global positions, from the shard
 // rank and the global lengths).
 //
-// Design: persistent 2-CTA clusters, one CTA per SM, 192 threads each:
+// Design: persistent 2-CTA clusters, one CTA per SM, 320 threads each:
 //   warp 0      TMA producer: this CTA's share of every KV tile (64 local rows)
-//               into a ring of tile slots, and (CTA 0) the query's 64 rope dims
-//               once per segment.
+//               into a ring of tile slots; the query's shared-memory operands
+//               once per segment.  The warp fetches block-table entries 32
+//               tiles at a time.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
-//   warps 2-5   load this CTA's half of the query's c_K dims into TMEM once per
-//               segment, then softmax (one query row per thread) and epilogue.
+//   warps 2-5   load this CTA's query chunks into TMEM once per segment, then
+//               softmax (one query row per thread) and epilogue.
+//   warps 6-9   send each partial score tile to the peer CTA.
 // A cluster handles a group of at most 128 query rows.  The 576 key dims are
 // split between the two CTAs: CTA r loads value chunks 4r .. 4r + 3 (dims
-// [256 r, 256 r + 256), 128-byte swizzled boxes of 64 rows x 64 dims) and CTA 0
-// also the rope chunk.  Per tile j, in each CTA:
-//   S_j^r = Q[:, K_r] K_j[:, K_r]^T   M=128 rows (A: TMEM; rope part from smem),
-//                                     N=64 KV rows, K=256 (+64)     -> TMEM fp32
-//   the two partial score tiles are swapped through distributed shared memory
-//   (st.async, credited on the receiver's mbarrier) and each CTA forms
-//   S_j = S_j^0 + S_j^1 (fp32 addition is commutative, so both CTAs hold the same
-//   bits and take the same softmax decisions);
+// [256 r, 256 r + 256), 128-byte swizzled boxes of 64 rows x 64 dims) and rope
+// dims [512 + 32 r, 512 + 32 r + 32) (64-byte swizzle).  Per tile j, in each CTA:
+//   S_j^r = Q[:, K_r] K_j[:, K_r]^T   M=128 rows, N=64 KV rows, K=288: query
+//                                     chunks 4r..4r+2 from TMEM, chunk 4r+3 and
+//                                     the rope half from shared memory -> TMEM fp32
+//   the sender warps push S_j^r to the peer (st.async, credited on the peer's
+//   mbarrier, two exchange buffers) and each CTA forms S_j = S_j^0 + S_j^1
+//   (fp32 addition is commutative, so both CTAs hold the same bits and take
+//   the same softmax decisions);
 //   P_j   = exp2(S_j*scale*log2e - m)  online softmax with lazy rescaling,
-//                                     written back over S_j as bf16 pairs
+//                                     bf16 pairs in their own TMEM columns
 //   O_r  += P_j V_j[:, dims of r]     M=128 rows (A = P from TMEM), N=256,
 //                                     K=64 KV rows                   -> TMEM fp32
 // Each KV byte crosses HBM once and reaches one SM's shared memory once; the
 // tile's chunks stay in the ring from the QK product to the PV product (V = the
-// first 512 dims of the same rows).  TMEM per CTA: O (256 columns), two S/P
-// tiles (2 x 64) and the query's c_K half (128).
+// first 512 dims of the same rows).  TMEM per CTA: O (256 columns), two S
+// tiles (2 x 64), P (32) and three query chunks (96).  An S tile is free as
+// soon as its sender and softmax warps have read it, so QK products run up to
+// two tiles ahead of the softmax while the exchange is in flight.
 //
 // Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
 // concatenation of all units' tiles is cut into V equal ranges, one per cluster
