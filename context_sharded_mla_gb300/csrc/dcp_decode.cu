@@ -841,8 +841,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------- fixup
 // Writes empty units (o = 0, lse = -inf) and merges the pieces of units cut by
-// range boundaries.  One block per unit.
-__global__ void __launch_bounds__(256) fixup_kernel(TcArgs a) {
+// range boundaries (the same LSE rule as the shard merge, base 2).  One block
+// per unit: its piece list is built once in shared memory, then one warp per
+// query row merges the pieces with 16-byte loads and stores (lane l owns dims
+// [16 l, 16 l + 16)).
+constexpr int kFixupThreads = 256;
+constexpr int kMaxPieces = 512;
+
+__global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
+  __shared__ int32_t piece_s[kMaxPieces];
+  __shared__ int32_t npiece_s;
   const int32_t U = a.B * a.n_held;
   const int32_t u = blockIdx.x;
   if (u >= U) return;
@@ -850,59 +858,89 @@ __global__ void __launch_bounds__(256) fixup_kernel(TcArgs a) {
   const int64_t s = a.tile_start[u], e = a.tile_start[u + 1];
   const int64_t T = a.tile_start[U];
   const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total;
-  const int64_t nelem = (int64_t)a.R_total * kDv;
-  if (s == e) {
-    for (int64_t i = threadIdx.x; i < nelem; i += blockDim.x) {
-      if (a.o_bf16) static_cast<__nv_bfloat16*>(a.o_part)[out_row0 * kDv + i] = __float2bfloat16_rn(0.f);
-      else static_cast<float*>(a.o_part)[out_row0 * kDv + i] = 0.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kFixupThreads / 32;
+  auto store_row = [&](int64_t orow, const float (&v)[16]) {
+    if (a.o_bf16) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + orow * kDv + 16 * lane);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 t = __floats2bfloat162_rn(v[8 * h + 2 * i], v[8 * h + 2 * i + 1]);
+          w[i] = *reinterpret_cast<uint32_t*>(&t);
+        }
+        dst[h] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o_part) + orow * kDv + 16 * lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
-    for (int i = threadIdx.x; i < a.R_total; i += blockDim.x) a.lse_part[out_row0 + i] = -INFINITY;
+  };
+  if (s == e) {
+    float z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+    for (int row = warp; row < a.R_total; row += kWarps) {
+      store_row(out_row0 + row, z);
+      if (lane == 0) a.lse_part[out_row0 + row] = -INFINITY;
+    }
     return;
   }
   const int V = a.V;
-  auto part_of = [&](int64_t x) {  // range containing tile x
-    int vv = (int)((x * V) / T);
-    while (vv + 1 < V && range_lo(T, vv + 1, V) <= x) ++vv;
-    while (vv > 0 && range_lo(T, vv, V) > x) --vv;
-    return vv;
-  };
-  const int v0 = part_of(s), v1 = part_of(e - 1);
-  if (v0 == v1) return;  // written whole by the main kernel
-  // each thread handles (row, 4 dims) items
-  for (int64_t item = threadIdx.x; item < (int64_t)a.R_total * (kDv / 4); item += blockDim.x) {
-    const int row = (int)(item / (kDv / 4));
-    const int d4 = (int)(item % (kDv / 4)) * 4;
-    float m = -INFINITY;
-    for (int vv = v0; vv <= v1; ++vv) {
-      if (range_lo(T, vv, V) == range_lo(T, vv + 1, V)) continue;  // empty range: no piece
-      const int k = range_lo(T, vv, V) >= s ? 0 : 1;
-      m = fmaxf(m, a.piece_lse[(int64_t)(2 * vv + k) * a.R_total + row]);
+  if (threadIdx.x == 0) {
+    auto part_of = [&](int64_t x) {  // range containing tile x
+      int vv = (int)((x * V) / T);
+      while (vv + 1 < V && range_lo(T, vv + 1, V) <= x) ++vv;
+      while (vv > 0 && range_lo(T, vv, V) > x) --vv;
+      return vv;
+    };
+    const int v0 = part_of(s), v1 = part_of(e - 1);
+    int n = 0;
+    if (v0 != v1) {
+      for (int vv = v0; vv <= v1 && n < kMaxPieces; ++vv) {
+        const int64_t rlo = range_lo(T, vv, V);
+        if (rlo == range_lo(T, vv + 1, V)) continue;  // empty range: no piece
+        piece_s[n++] = 2 * vv + (rlo >= s ? 0 : 1);
+      }
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    npiece_s = n;
+  }
+  __syncthreads();
+  const int np = npiece_s;
+  if (np == 0) return;  // written whole by the main kernel
+  for (int row = warp; row < a.R_total; row += kWarps) {
+    float m = -INFINITY;
+    for (int k = 0; k < np; ++k) m = fmaxf(m, a.piece_lse[(int64_t)piece_s[k] * a.R_total + row]);
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
-      for (int vv = v0; vv <= v1; ++vv) {
-        if (range_lo(T, vv, V) == range_lo(T, vv + 1, V)) continue;
-        const int k = range_lo(T, vv, V) >= s ? 0 : 1;
-        const int64_t pr = (int64_t)(2 * vv + k) * a.R_total + row;
+      for (int k = 0; k < np; ++k) {
+        const int64_t pr = (int64_t)piece_s[k] * a.R_total + row;
         const float lv = a.piece_lse[pr];
         if (lv == -INFINITY) continue;
         const float w = exp2f(lv - m);
         wsum += w;
-        const float4 o4 = *reinterpret_cast<const float4*>(a.piece_o + pr * kDv + d4);
-        acc[0] = fmaf(w, o4.x, acc[0]);
-        acc[1] = fmaf(w, o4.y, acc[1]);
-        acc[2] = fmaf(w, o4.z, acc[2]);
-        acc[3] = fmaf(w, o4.w, acc[3]);
+        const float4* src = reinterpret_cast<const float4*>(a.piece_o + pr * kDv + 16 * lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 o4 = src[i];
+          acc[4 * i] = fmaf(w, o4.x, acc[4 * i]);
+          acc[4 * i + 1] = fmaf(w, o4.y, acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(w, o4.z, acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(w, o4.w, acc[4 * i + 3]);
+        }
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int64_t o_idx = (out_row0 + row) * kDv + d4;
-    for (int i = 0; i < 4; ++i) {
-      if (a.o_bf16) static_cast<__nv_bfloat16*>(a.o_part)[o_idx + i] = __float2bfloat16_rn(acc[i] * inv);
-      else static_cast<float*>(a.o_part)[o_idx + i] = acc[i] * inv;
-    }
-    if (d4 == 0) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] *= inv;
+    store_row(out_row0 + row, acc);
+    if (lane == 0) {
       const float lse2 = wsum > 0.f ? m + log2f(wsum) : -INFINITY;
       a.lse_part[out_row0 + row] = a.base2 ? lse2 : lse2 * kLn2;
     }
@@ -1088,7 +1126,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
   partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, a);
-  fixup_kernel<<<U, 256, 0, st>>>(a);
+  fixup_kernel<<<U, kFixupThreads, 0, st>>>(a);
   return launch_status(3);
 }
 
