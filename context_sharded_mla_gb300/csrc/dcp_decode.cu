@@ -71,9 +71,9 @@ constexpr int kThreads = 320;                 // 10 warps: producer, MMA issuer,
 constexpr int kMaxGroupRows = 128;
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
 constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns
-constexpr uint32_t kPCol = 384;               // [384, 416): P of one tile as bf16 pairs
-constexpr uint32_t kQCol = 416;               // [416, 512): query chunks 4r .. 4r + 2 as bf16 pairs
-constexpr int kQTmemChunks = 3;               // query chunk 4r + 3 is read from shared memory
+constexpr uint32_t kPCol = 384;               // [384, 448): P of two tiles as bf16 pairs (2 x 32)
+constexpr uint32_t kQCol = 448;               // [448, 512): query chunks 4r, 4r + 1 as bf16 pairs
+constexpr int kQTmemChunks = 2;               // query chunks 4r + 2, 4r + 3 are read from shared memory
 constexpr int kXRowBytes = kTile * 4;         // one row of a partial score tile (fp32)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -110,9 +110,12 @@ __host__ __device__ inline uint32_t round1024(uint32_t v) { return (v + 1023u) &
 
 __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   SmemLayout s;
-  s.qc = 0;                                        // query chunk 4r + 3: [128][64] bf16, 128-byte swizzle
-  s.qr = 128 * 128;                                // query rope dims [32r, 32r + 32): [128][32], 64-byte swizzle
-  s.x = s.qr + 128 * 64;                           // the peer's partial scores, two buffers of [Rg][64] fp32
+  // The M = 128 shared-memory A operands hold only the group's Rg rows; the
+  // products also read the 128 - Rg rows that follow (whatever lies there) into
+  // TMEM lanes no thread reads back.
+  s.qc = 0;                                        // query chunks 4r + 2, 4r + 3: [Rg][64] bf16 each, 128-byte swizzle
+  s.qr = 2 * (uint32_t)Rg * 128;                   // query rope dims [32r, 32r + 32): [Rg][32], 64-byte swizzle
+  s.x = round1024(s.qr + (uint32_t)Rg * 64);       // the peer's partial scores, two buffers of [Rg][64] fp32
   s.xbuf = round1024((uint32_t)Rg * kXRowBytes);
   s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
   s.rope = s.ring;                                 // (kept for the layout struct; rope lives in the slots)
@@ -220,6 +223,32 @@ struct SegIter {
 
 __device__ inline int64_t range_lo(int64_t T, int v, int V) { return (T * v) / V; }
 
+// Two fp32 values in one 64-bit register pair, for the packed FP32 operations
+// of sm_100 (two lanes per instruction; each lane rounds as its scalar form).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22,
 // 2^-inf = +0); the result is rounded to bf16 for the PV product anyway.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -310,8 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
   // query rows past the group are read by the M = 128 products: zeros
-  for (int i = tid; i < (128 * 128 + 128 * 64) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(qc_s)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (int)(sl.x / 16); i += kThreads) reinterpret_cast<uint4*>(qc_s)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_base_s, 512);
@@ -437,8 +465,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!warp_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s, lane)) { ok = false; break; }
         if (lane == 0) {
           const int32_t qy = b * a.R_total + g * Rg;
-          mbar_arrive_expect_tx(&bars[kQFull], Rg * (128 + 64));
-          tma_load_2d(qc_s, &tmap_q, &bars[kQFull], (kOwnChunks * (int)rank + kQTmemChunks) * kChunkDims, qy);
+          mbar_arrive_expect_tx(&bars[kQFull], Rg * (2 * 128 + 64));
+          for (int i = kQTmemChunks; i < kOwnChunks; ++i)
+            tma_load_2d(qc_s + (i - kQTmemChunks) * Rg * 128, &tmap_q, &bars[kQFull],
+                        (kOwnChunks * (int)rank + i) * kChunkDims, qy);
           tma_load_2d(qr_s, &tmap_q64, &bars[kQFull], 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, qy);
         }
         ++seg;
@@ -492,14 +522,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_bf16_ts(d, tmem + kQCol + 32 * i + 8 * kk, kd + i * (kChunkBytes >> 4) + 2 * kk, idesc_qk,
                         (i | kk) != 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(d, qcdesc0 + 2 * kk, kd + kQTmemChunks * (kChunkBytes >> 4) + 2 * kk, idesc_qk, 1);
+        for (int i = kQTmemChunks; i < kOwnChunks; ++i)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, qcdesc0 + (i - kQTmemChunks) * ((Rg * 128) >> 4) + 2 * kk,
+                        kd + i * (kChunkBytes >> 4) + 2 * kk, idesc_qk, 1);
 #pragma unroll
         for (int kk = 0; kk < kRopeHalf / 16; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rdesc0 + soff + 2 * kk, idesc_qk, 1);
         mma_commit(&bars[kSFull0 + (j & 1)]);
       };
       auto issue_pv = [&](uint32_t j, uint32_t ts, bool first) {
-        const uint32_t pa = tmem + kPCol;  // P: 64 bf16 = 32 columns
+        const uint32_t pa = tmem + kPCol + 32 * (j & 1);  // P(j): 64 bf16 = 32 columns
         const uint64_t vd = vdesc0 + ((ts * kSlotBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -691,10 +724,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const uint4 w4 = ld_shared_v4(src + ((uint32_t)(i ^ (c & 15)) << 4));
-              s[4 * i] = __float_as_uint(__uint_as_float(s[4 * i]) + __uint_as_float(w4.x));
-              s[4 * i + 1] = __float_as_uint(__uint_as_float(s[4 * i + 1]) + __uint_as_float(w4.y));
-              s[4 * i + 2] = __float_as_uint(__uint_as_float(s[4 * i + 2]) + __uint_as_float(w4.z));
-              s[4 * i + 3] = __float_as_uint(__uint_as_float(s[4 * i + 3]) + __uint_as_float(w4.w));
+              const uint64_t a0 = f2_add(f2_pack(s[4 * i], s[4 * i + 1]), f2_pack(w4.x, w4.y));
+              const uint64_t a1 = f2_add(f2_pack(s[4 * i + 2], s[4 * i + 3]), f2_pack(w4.z, w4.w));
+              f2_unpack(a0, s[4 * i], s[4 * i + 1]);
+              f2_unpack(a1, s[4 * i + 2], s[4 * i + 3]);
             }
           }
           // The adds above consumed every lane's reads, so the buffer is free once
@@ -717,9 +750,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(s[k]);
 #pragma unroll
-          for (int k = 8; k < 64; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(s[k]));
-          const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int k = 8; k < 64; k += 2)
+            mx[((k - 8) >> 1) & 7] = fmax3(mx[((k - 8) >> 1) & 7], __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
+          const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
           const float mt = mraw * a.scale_log2;  // scale > 0: the max commutes with the scaling
           bool need = false;
           float alpha = 1.f;
@@ -730,13 +763,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             alpha = exp2f(m_ref - mt);
             m_ref = mt;
           }
-          // PV(j - 1) must be done before O is rescaled or P is overwritten
-          bool pv_prev_done = j == 0;
-          if (__any_sync(0xffffffffu, need)) {
-            // rows whose maximum moved: scale their O row
+          if (__any_sync(0xffffffffu, need && has_x)) {
+            // rows whose maximum moved: scale their O row once PV(j - 1) is done
             // (a row's maximum is finite only after a tile of this segment, so j >= 1)
             if (!wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
-            pv_prev_done = true;
             tc_fence_after();
 #pragma unroll 1
             for (int q = 0; q < 8; ++q) {
@@ -753,21 +783,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           const float cs = a.scale_log2;
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint64_t cs2 = f2_pack(__float_as_uint(cs), __float_as_uint(cs));
+          const uint64_t nm2 = f2_pack(__float_as_uint(-m_use), __float_as_uint(-m_use));
+          uint64_t ps[4] = {0, 0, 0, 0};  // pairs of partial row sums (+0.f bits)
           uint32_t pk[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(s[2 * k]), cs, -m_use));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(s[2 * k + 1]), cs, -m_use));
-            ps[k & 3] += p0 + p1;
+            uint32_t x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), cs2, nm2), x0, x1);
+            const float p0 = fast_exp2(__uint_as_float(x0));
+            const float p1 = fast_exp2(__uint_as_float(x1));
+            ps[k & 3] = f2_add(ps[k & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
             __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             pk[k] = *reinterpret_cast<uint32_t*>(&h);
           }
-          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          // P -> TMEM (A operand of the PV product) once PV(j - 1) has read the previous P
-          if (!pv_prev_done && !wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
+          {
+            uint32_t a0, a1;
+            f2_unpack(f2_add(f2_add(ps[0], ps[1]), f2_add(ps[2], ps[3])), a0, a1);
+            l += __uint_as_float(a0) + __uint_as_float(a1);
+          }
+          // P(j) -> TMEM (A operand of the PV product) once PV(j - 2) has read
+          // the buffer's previous contents
+          if (j >= 2 && !wwait(&bars[kPVDone0 + (j & 1)], ((j - 2) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          tmem_st32(tmem + lane_base + kPCol, pk);
+          tmem_st32(tmem + lane_base + kPCol + 32 * (j & 1), pk);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
