@@ -115,7 +115,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   // TMEM lanes no thread reads back.
   s.qc = 0;                                        // query chunks 4r + 2, 4r + 3: [Rg][64] bf16 each, 128-byte swizzle
   s.qr = 2 * (uint32_t)Rg * 128;                   // query rope dims [32r, 32r + 32): [Rg][32], 64-byte swizzle
-  s.x = round1024(s.qr + (uint32_t)Rg * 64);       // the peer's partial scores, two buffers of [Rg][64] fp32
+  s.x = round1024(s.qr + (uint32_t)Rg * 64);       // [Rg][64] fp32: the peer's partial scores, then my staged ones
   s.xbuf = round1024((uint32_t)Rg * kXRowBytes);
   s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
   s.rope = s.ring;                                 // (kept for the layout struct; rope lives in the slots)
@@ -126,7 +126,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
 }
 
 enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
-           kXFull0, kXFull1, kXEmpty0, kXEmpty1, kNumFixedBars };
+           kXFull, kXEmpty, kStaged, kNumFixedBars };
 static_assert(kNumFixedBars <= 16, "fixed barriers");
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
@@ -325,16 +325,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kPFull0], nact);
     mbar_init(&bars[kPFull1], nact);
     mbar_init(&bars[kOFree], nact);
-    mbar_init(&bars[kXEmpty0], nact);  // remote arrivals: the peer's warps have read my scores
-    mbar_init(&bars[kXEmpty1], nact);
+    mbar_init(&bars[kXEmpty], nact);  // remote arrivals: the peer's warps have read my scores
+    mbar_init(&bars[kStaged], nact);  // sender warps have staged a partial score tile
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 1);
     }
     fence_barrier_init();
-    // the peer's first two partial tiles are expected before they can be sent
-    for (uint32_t j = 0; j < 2 && j < ntiles_cta; ++j)
-      mbar_arrive_expect_tx(&bars[kXFull0 + j], (uint32_t)Rg * kXRowBytes);
+    // the peer's first partial tile is expected before it can be sent
+    if (ntiles_cta > 0) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
@@ -615,16 +614,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------------ score senders
-    // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32): each tile's partial scores
-    // go to the peer's exchange buffer (16-byte pieces, 256-byte rows swizzled by
-    // row so a warp's stores spread over all banks), off the softmax warps' path.
+    // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
+    // scores and stages them in shared memory (256-byte rows, 16-byte pieces
+    // swizzled by row so a warp's stores spread over all banks); lane 0 of the
+    // quarter-0 warp then ships the whole tile to the peer's receive buffer with
+    // one bulk copy, so the slow cluster network never holds up the
+    // shared-memory pipe the softmax warps read through.  The staging buffer is
+    // reused once the peer has read the previous tile (which implies the copy
+    // has landed).
     const int c = 32 * (warp & 3) + lane;
     if (32 * (warp & 3) < Rg && lo < hi) {
       const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
       const bool has_x = c < Rg;
       const uint32_t peer = rank ^ 1u;
-      const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer) + (uint32_t)c * kXRowBytes;
-      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull0]), peer);
+      unsigned char* stage = x_s + sl.xbuf;
+      const uint32_t stage_row = smem_u32(stage) + (uint32_t)c * kXRowBytes;
+      const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer);
+      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull]), peer);
       for (uint32_t j = 0; j < ntiles_cta; ++j) {
         uint32_t s[64];
         if (!warp_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_s, lane)) break;
@@ -636,16 +642,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
-        // the peer has read what was sent for tile j - 2 (two exchange buffers)
-        const uint32_t xb = j & 1;
-        if (!warp_wait_cluster(&bars[kXEmpty0 + xb], ((j >> 1) & 1) ^ 1, abort_s, lane)) break;
+        // the peer has read tile j - 1: its receive buffer and my staging buffer are free
+        if (!warp_wait_cluster(&bars[kXEmpty], (j & 1) ^ 1, abort_s, lane)) break;
         if (has_x) {
-          const uint32_t dst = x_peer + xb * sl.xbuf;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            st_async_v4(dst + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3],
-                        xfull_peer + 8 * xb);
+            st_shared_v4(stage_row + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2],
+                         s[4 * i + 3]);
         }
+        fence_proxy_async_smem();  // the copy engine reads the staged rows
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kStaged]);
+        int sent = 1;
+        if ((warp & 3) == 0 && lane == 0) {
+          sent = mbar_wait(&bars[kStaged], j & 1, abort_s) ? 1 : 0;
+          if (sent) bulk_copy_to_peer(x_peer, stage, (uint32_t)Rg * kXRowBytes, xfull_peer);
+        }
+        if (!__shfl_sync(0xffffffffu, sent, 0)) break;
       }
     }
   } else if (32 * (warp & 3) < Rg) {
@@ -656,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const bool has_x = c < Rg;  // this row's partial scores cross between the CTAs
     const uint32_t peer = rank ^ 1u;
-    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty0]), peer);
+    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty]), peer);
     const uint32_t x_mine = smem_u32(x_s) + (uint32_t)c * kXRowBytes;
     if (lo < hi) {
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_s, lane); };
@@ -717,10 +730,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
           // ---- the peer's partial scores of tile j: S = mine + peer's
-          const uint32_t xb = j & 1;
-          if (!wwait_cluster(&bars[kXFull0 + xb], (j >> 1) & 1)) { ok = false; break; }
+          if (!wwait_cluster(&bars[kXFull], j & 1)) { ok = false; break; }
           if (has_x) {
-            const uint32_t src = x_mine + xb * sl.xbuf;
+            const uint32_t src = x_mine;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const uint4 w4 = ld_shared_v4(src + ((uint32_t)(i ^ (c & 15)) << 4));
@@ -734,9 +746,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the warp has passed this point; the release to the peer needs no fence.
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_cluster_relaxed(xempty_peer + 8 * xb);
-            // the next phase of this receive buffer expects the peer's tile j + 2
-            if (warp == 4 && j + 2 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull0 + xb], (uint32_t)Rg * kXRowBytes);
+            mbar_arrive_cluster_relaxed(xempty_peer);
+            // the next phase of the receive buffer expects the peer's tile j + 1
+            if (warp == 4 && j + 1 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
           }
           // ---- online softmax of tile j
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
