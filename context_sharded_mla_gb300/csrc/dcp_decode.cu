@@ -25,8 +25,9 @@
 //   S_j^r = Q[:, K_r] K_j[:, K_r]^T   M=128 rows, N=64 KV rows, K=288: query
 //                                     chunks 4r..4r+2 from TMEM, chunk 4r+3 and
 //                                     the rope half from shared memory -> TMEM fp32
-//   the sender warps push S_j^r to the peer (st.async, credited on the peer's
-//   mbarrier, two exchange buffers) and each CTA forms S_j = S_j^0 + S_j^1
+//   the sender warps stage S_j^r in shared memory and one bulk copy ships it to
+//   the peer (credited on the peer's mbarrier; two buffers per CTA swap the
+//   staging and receiving roles every tile) and each CTA forms S_j = S_j^0 + S_j^1
 //   (fp32 addition is commutative, so both CTAs hold the same bits and take
 //   the same softmax decisions);
 //   P_j   = exp2(S_j*scale*log2e - m)  online softmax with lazy rescaling,
@@ -115,7 +116,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   // TMEM lanes no thread reads back.
   s.qc = 0;                                        // query chunks 4r + 2, 4r + 3: [Rg][64] bf16 each, 128-byte swizzle
   s.qr = 2 * (uint32_t)Rg * 128;                   // query rope dims [32r, 32r + 32): [Rg][32], 64-byte swizzle
-  s.x = round1024(s.qr + (uint32_t)Rg * 64);       // [Rg][64] fp32: the peer's partial scores, then my staged ones
+  s.x = round1024(s.qr + (uint32_t)Rg * 64);       // two [Rg][64] fp32 buffers: partial scores staged / received
   s.xbuf = round1024((uint32_t)Rg * kXRowBytes);
   s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
   s.rope = s.ring;                                 // (kept for the layout struct; rope lives in the slots)
@@ -126,7 +127,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
 }
 
 enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
-           kXFull, kXEmpty, kStaged, kNumFixedBars };
+           kXFull0, kXFull1, kXRead0, kXRead1, kStaged, kNumFixedBars };
 static_assert(kNumFixedBars <= 16, "fixed barriers");
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
@@ -325,15 +326,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kPFull0], nact);
     mbar_init(&bars[kPFull1], nact);
     mbar_init(&bars[kOFree], nact);
-    mbar_init(&bars[kXEmpty], nact);  // remote arrivals: the peer's warps have read my scores
+    // the softmax warps have read the peer's partial scores out of receive buffer 0 / 1
+    // (one barrier per buffer: a single one could run two phases ahead of the
+    // sender waiting on it, since the peer's next tile may arrive and be read first)
+    mbar_init(&bars[kXRead0], nact);
+    mbar_init(&bars[kXRead1], nact);
     mbar_init(&bars[kStaged], nact);  // sender warps have staged a partial score tile
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 1);
     }
     fence_barrier_init();
-    // the peer's first partial tile is expected before it can be sent
-    if (ntiles_cta > 0) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
+    // tile j's partial scores from the peer land in buffer (j & 1) ^ 1: expect tiles 0 and 1
+    for (uint32_t j = 0; j < 2 && j < ntiles_cta; ++j)
+      mbar_arrive_expect_tx(&bars[kXFull0 + ((j & 1) ^ 1)], (uint32_t)Rg * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
@@ -617,20 +623,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
     // scores and stages them in shared memory (256-byte rows, 16-byte pieces
     // swizzled by row so a warp's stores spread over all banks); lane 0 of the
-    // quarter-0 warp then ships the whole tile to the peer's receive buffer with
-    // one bulk copy, so the slow cluster network never holds up the
-    // shared-memory pipe the softmax warps read through.  The staging buffer is
-    // reused once the peer has read the previous tile (which implies the copy
-    // has landed).
+    // quarter-0 warp then ships the whole tile to the peer with one bulk copy,
+    // so the slow cluster network never holds up the shared-memory pipe the
+    // softmax warps read through.  Two buffers per CTA swap roles every tile:
+    // tile j is staged in buffer j & 1 and the peer's tile j lands in buffer
+    // (j & 1) ^ 1.  Both conditions for tile j are local: my buffer j & 1 held
+    // the peer's tile j - 1, which my softmax warps have read; the peer's buffer
+    // (j & 1) ^ 1 held its staged tile j - 1, whose copy to me has landed (it
+    // was read here).
     const int c = 32 * (warp & 3) + lane;
     if (32 * (warp & 3) < Rg && lo < hi) {
       const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
       const bool has_x = c < Rg;
       const uint32_t peer = rank ^ 1u;
-      unsigned char* stage = x_s + sl.xbuf;
-      const uint32_t stage_row = smem_u32(stage) + (uint32_t)c * kXRowBytes;
       const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer);
-      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull]), peer);
+      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull0]), peer);
       for (uint32_t j = 0; j < ntiles_cta; ++j) {
         uint32_t s[64];
         if (!warp_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_s, lane)) break;
@@ -642,9 +649,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
-        // the peer has read tile j - 1: its receive buffer and my staging buffer are free
-        if (!warp_wait_cluster(&bars[kXEmpty], (j & 1) ^ 1, abort_s, lane)) break;
+        // my softmax warps have read the peer's tile j - 1 out of buffer j & 1
+        const uint32_t sb = j & 1;
+        if (j > 0 && !warp_wait(&bars[kXRead0 + sb], ((j - 1) >> 1) & 1, abort_s, lane)) break;
+        unsigned char* stage = x_s + sb * sl.xbuf;
         if (has_x) {
+          const uint32_t stage_row = smem_u32(stage) + (uint32_t)c * kXRowBytes;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             st_shared_v4(stage_row + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2],
@@ -656,7 +666,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int sent = 1;
         if ((warp & 3) == 0 && lane == 0) {
           sent = mbar_wait(&bars[kStaged], j & 1, abort_s) ? 1 : 0;
-          if (sent) bulk_copy_to_peer(x_peer, stage, (uint32_t)Rg * kXRowBytes, xfull_peer);
+          if (sent)
+            bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf, stage, (uint32_t)Rg * kXRowBytes, xfull_peer + 8 * (sb ^ 1));
         }
         if (!__shfl_sync(0xffffffffu, sent, 0)) break;
       }
@@ -668,8 +679,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int c = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const bool has_x = c < Rg;  // this row's partial scores cross between the CTAs
-    const uint32_t peer = rank ^ 1u;
-    const uint32_t xempty_peer = mapa_shared(smem_u32(&bars[kXEmpty]), peer);
     const uint32_t x_mine = smem_u32(x_s) + (uint32_t)c * kXRowBytes;
     if (lo < hi) {
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_s, lane); };
@@ -730,9 +739,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
           // ---- the peer's partial scores of tile j: S = mine + peer's
-          if (!wwait_cluster(&bars[kXFull], j & 1)) { ok = false; break; }
+          const uint32_t rb = (j & 1) ^ 1;  // receive buffer of tile j
+          if (!wwait_cluster(&bars[kXFull0 + rb], (j >> 1) & 1)) { ok = false; break; }
           if (has_x) {
-            const uint32_t src = x_mine;
+            const uint32_t src = x_mine + rb * sl.xbuf;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const uint4 w4 = ld_shared_v4(src + ((uint32_t)(i ^ (c & 15)) << 4));
@@ -742,13 +752,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               f2_unpack(a1, s[4 * i + 2], s[4 * i + 3]);
             }
           }
-          // The adds above consumed every lane's reads, so the buffer is free once
-          // the warp has passed this point; the release to the peer needs no fence.
+          // The adds above consumed every lane's reads: the buffer may be restaged.
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_cluster_relaxed(xempty_peer);
-            // the next phase of the receive buffer expects the peer's tile j + 1
-            if (warp == 4 && j + 1 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull], (uint32_t)Rg * kXRowBytes);
+            mbar_arrive(&bars[kXRead0 + rb]);
+            // the next phase of this receive buffer expects the peer's tile j + 2
+            if (warp == 4 && j + 2 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull0 + rb], (uint32_t)Rg * kXRowBytes);
           }
           // ---- online softmax of tile j
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
