@@ -127,7 +127,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
 }
 
 enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
-           kXFull0, kXFull1, kXRead0, kXRead1, kStaged, kNumFixedBars };
+           kXFull0, kXFull1, kXRead0, kXRead1, kNumFixedBars };
 static_assert(kNumFixedBars <= 16, "fixed barriers");
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
@@ -331,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // sender waiting on it, since the peer's next tile may arrive and be read first)
     mbar_init(&bars[kXRead0], nact);
     mbar_init(&bars[kXRead1], nact);
-    mbar_init(&bars[kStaged], nact);  // sender warps have staged a partial score tile
+
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 1);
@@ -621,11 +621,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= 6) {
     // ------------------------------------------------------------------ score senders
     // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
-    // scores and stages them in shared memory (256-byte rows, 16-byte pieces
-    // swizzled by row so a warp's stores spread over all banks); lane 0 of the
-    // quarter-0 warp then ships the whole tile to the peer with one bulk copy,
-    // so the slow cluster network never holds up the shared-memory pipe the
-    // softmax warps read through.  Two buffers per CTA swap roles every tile:
+    // scores, stages them in shared memory (256-byte rows, 16-byte pieces
+    // swizzled by row so a warp's stores spread over all banks) and ships its
+    // rows to the peer with one bulk copy, so the slow cluster network never
+    // holds up the shared-memory pipe the softmax warps read through.  Two buffers per CTA swap roles every tile:
     // tile j is staged in buffer j & 1 and the peer's tile j lands in buffer
     // (j & 1) ^ 1.  Both conditions for tile j are local: my buffer j & 1 held
     // the peer's tile j - 1, which my softmax warps have read; the peer's buffer
@@ -662,14 +661,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();  // the copy engine reads the staged rows
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kStaged]);
-        int sent = 1;
-        if ((warp & 3) == 0 && lane == 0) {
-          sent = mbar_wait(&bars[kStaged], j & 1, abort_s) ? 1 : 0;
-          if (sent)
-            bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf, stage, (uint32_t)Rg * kXRowBytes, xfull_peer + 8 * (sb ^ 1));
+        if (lane == 0) {
+          // this warp's rows [32 q, 32 q + rows) go out as one copy; the peer's
+          // barrier expects the bytes of all the warps' copies
+          const uint32_t r0 = 32 * (warp & 3);
+          const uint32_t rows = min(32, Rg - (int)r0);
+          bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf + r0 * kXRowBytes, stage + r0 * kXRowBytes,
+                            rows * kXRowBytes, xfull_peer + 8 * (sb ^ 1));
         }
-        if (!__shfl_sync(0xffffffffu, sent, 0)) break;
       }
     }
   } else if (32 * (warp & 3) < Rg) {
