@@ -68,6 +68,7 @@ constexpr int kRopeHalfBytes = kTile * 64;
 constexpr int kRopeOff = kOwnChunks * kChunkBytes;         // rope part inside a tile slot
 constexpr int kSlotBytes = kRopeOff + kRopeHalfBytes;      // 36 KB per tile slot
 constexpr int kMaxTileSlots = 8;
+constexpr int kFixedBarSlots = 32;            // mbarriers other than the per-slot ones
 constexpr int kThreads = 320;                 // 10 warps: producer, MMA issuer, 4 softmax/epilogue, 4 senders
 constexpr int kMaxGroupRows = 128;
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
@@ -121,14 +122,16 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
   s.rope = s.ring;                                 // (kept for the layout struct; rope lives in the slots)
   s.bars = s.ring + nts * kSlotBytes;
-  s.misc = s.bars + (16 + 2 * kMaxTileSlots) * 8;
+  s.misc = s.bars + (kFixedBarSlots + 2 * kMaxTileSlots) * 8;
   s.total = s.misc + 64;
   return s;
 }
 
 enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
-           kXFull0, kXFull1, kXRead0, kXRead1, kNumFixedBars };
-static_assert(kNumFixedBars <= 16, "fixed barriers");
+           kXFull = 11,  // [2 buffers][4 row quarters]: the peer's rows of a quarter have landed
+           kXRead = 19,  // [2 buffers][4 row quarters]: my softmax warp of the quarter has read them
+           kNumFixedBars = 27 };
+static_assert(kNumFixedBars <= kFixedBarSlots, "fixed barriers");
 
 __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* bad) {
   const int64_t S = a.seq_lens[b];
@@ -297,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   unsigned char* x_s = smem + sl.x;
   unsigned char* ring = smem + sl.ring;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
-  uint64_t* tfull = bars + 16;                  // tile slot landed
+  uint64_t* tfull = bars + kFixedBarSlots;      // tile slot landed
   uint64_t* tempty = tfull + kMaxTileSlots;     // tile slot released by its PV product
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + sl.misc);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + sl.misc + 4);
@@ -326,11 +329,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kPFull0], nact);
     mbar_init(&bars[kPFull1], nact);
     mbar_init(&bars[kOFree], nact);
-    // the softmax warps have read the peer's partial scores out of receive buffer 0 / 1
-    // (one barrier per buffer: a single one could run two phases ahead of the
-    // sender waiting on it, since the peer's next tile may arrive and be read first)
-    mbar_init(&bars[kXRead0], nact);
-    mbar_init(&bars[kXRead1], nact);
+    // The score exchange runs as one channel per row quarter (a sender warp ships
+    // the rows of its TMEM lane quarter and the softmax warp of that quarter reads
+    // them): one "landed" and one "read" barrier per buffer and quarter, so no
+    // barrier can run two phases ahead of its waiter (all are single-arrival).
 
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
@@ -339,7 +341,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     // tile j's partial scores from the peer land in buffer (j & 1) ^ 1: expect tiles 0 and 1
     for (uint32_t j = 0; j < 2 && j < ntiles_cta; ++j)
-      mbar_arrive_expect_tx(&bars[kXFull0 + ((j & 1) ^ 1)], (uint32_t)Rg * kXRowBytes);
+      for (int q = 0; q < nact; ++q)
+        mbar_arrive_expect_tx(&bars[kXFull + 4 * ((j & 1) ^ 1) + q], (uint32_t)min(32, Rg - 32 * q) * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
@@ -636,7 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool has_x = c < Rg;
       const uint32_t peer = rank ^ 1u;
       const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer);
-      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull0]), peer);
+      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull + (warp & 3)]), peer);
       for (uint32_t j = 0; j < ntiles_cta; ++j) {
         uint32_t s[64];
         if (!warp_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_s, lane)) break;
@@ -650,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
         // my softmax warps have read the peer's tile j - 1 out of buffer j & 1
         const uint32_t sb = j & 1;
-        if (j > 0 && !warp_wait(&bars[kXRead0 + sb], ((j - 1) >> 1) & 1, abort_s, lane)) break;
+        if (j > 0 && !warp_wait(&bars[kXRead + 4 * sb + (warp & 3)], ((j - 1) >> 1) & 1, abort_s, lane)) break;
         unsigned char* stage = x_s + sb * sl.xbuf;
         if (has_x) {
           const uint32_t stage_row = smem_u32(stage) + (uint32_t)c * kXRowBytes;
@@ -667,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t r0 = 32 * (warp & 3);
           const uint32_t rows = min(32, Rg - (int)r0);
           bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf + r0 * kXRowBytes, stage + r0 * kXRowBytes,
-                            rows * kXRowBytes, xfull_peer + 8 * (sb ^ 1));
+                            rows * kXRowBytes, xfull_peer + 8 * 4 * (sb ^ 1));
         }
       }
     }
@@ -739,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
           // ---- the peer's partial scores of tile j: S = mine + peer's
           const uint32_t rb = (j & 1) ^ 1;  // receive buffer of tile j
-          if (!wwait_cluster(&bars[kXFull0 + rb], (j >> 1) & 1)) { ok = false; break; }
+          if (!wwait_cluster(&bars[kXFull + 4 * rb + (warp & 3)], (j >> 1) & 1)) { ok = false; break; }
           if (has_x) {
             const uint32_t src = x_mine + rb * sl.xbuf;
 #pragma unroll
@@ -754,9 +757,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // The adds above consumed every lane's reads: the buffer may be restaged.
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&bars[kXRead0 + rb]);
-            // the next phase of this receive buffer expects the peer's tile j + 2
-            if (warp == 4 && j + 2 < ntiles_cta) mbar_arrive_expect_tx(&bars[kXFull0 + rb], (uint32_t)Rg * kXRowBytes);
+            mbar_arrive(&bars[kXRead + 4 * rb + (warp & 3)]);
+            // the next phase of this buffer's quarter expects the peer's tile j + 2
+            if (j + 2 < ntiles_cta)
+              mbar_arrive_expect_tx(&bars[kXFull + 4 * rb + (warp & 3)],
+                                    (uint32_t)min(32, Rg - 32 * (warp & 3)) * kXRowBytes);
           }
           // ---- online softmax of tile j
           const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
