@@ -10,14 +10,14 @@
 // rank and the global lengths).
 //
 // Design: persistent 2-CTA clusters, one CTA per SM, 320 threads each:
-//   warp 0      TMA producer: this CTA's share of every KV tile (64 local rows)
+//   warp 10     TMA producer: this CTA's share of every KV tile (64 local rows)
 //               into a ring of tile slots; the query's shared-memory operands
 //               once per segment.  The warp fetches block-table entries 32
 //               tiles at a time.
-//   warp 1      tcgen05 issuer (one thread) and TMEM owner.
-//   warps 2-5   load this CTA's query chunks into TMEM once per segment, then
+//   warp 11     tcgen05 issuer (one thread) and TMEM owner.
+//   warps 0-3   load this CTA's query chunks into TMEM once per segment, then
 //               softmax (one query row per thread) and epilogue.
-//   warps 6-9   send each partial score tile to the peer CTA.
+//   warps 4-7   send each partial score tile to the peer CTA.
 // A cluster handles a group of at most 128 query rows.  The 576 key dims are
 // split between the two CTAs: CTA r loads value chunks 4r .. 4r + 3 (dims
 // [256 r, 256 r + 256), 128-byte swizzled boxes of 64 rows x 64 dims) and rope
@@ -69,7 +69,15 @@ constexpr int kRopeOff = kOwnChunks * kChunkBytes;         // rope part inside a
 constexpr int kSlotBytes = kRopeOff + kRopeHalfBytes;      // 36 KB per tile slot
 constexpr int kMaxTileSlots = 8;
 constexpr int kFixedBarSlots = 32;            // mbarriers other than the per-slot ones
-constexpr int kThreads = 320;                 // 10 warps: producer, MMA issuer, 4 softmax/epilogue, 4 senders
+constexpr int kThreads = 384;                 // 12 warps (roles below)
+// Warp roles.  Warp w runs on SM sub-partition w % 4 and reaches TMEM lanes
+// [32 (w % 4), 32 (w % 4) + 32): the softmax and sender warps of row quarter q
+// are q and 4 + q.  The tensor-core issuer (a polling thread) sits with the
+// warps of quarter 3, the quarter a group of up to 96 rows leaves empty, and
+// the producer with quarter 2; warps 8 and 9 have no role.
+constexpr int kSenderWarp0 = 4;
+constexpr int kProducerWarp = 10;
+constexpr int kMmaWarp = 11;
 constexpr int kMaxGroupRows = 128;
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
 constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns
@@ -349,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // query rows past the group are read by the M = 128 products: zeros
   for (int i = tid; i < (int)(sl.x / 16); i += kThreads) reinterpret_cast<uint4*>(qc_s)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_base_s, 512);
     tmem_relinquish();
   }
@@ -358,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
     // The whole warp walks the tile sequence: its lanes fetch the block-table
     // entries of 32 tiles at a time (the next 32 are already in flight), lane 0
@@ -503,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     // Event-driven single thread: QK(j) once tile j has landed and the S tile it
     // writes (last used by tile j - 2) has been read; PV(j) once P(j) is ready.
@@ -621,9 +629,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kSenderWarp0 && warp < kSenderWarp0 + 4) {
     // ------------------------------------------------------------------ score senders
-    // Warp 6 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
+    // Warp 4 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
     // scores, stages them in shared memory (256-byte rows, 16-byte pieces
     // swizzled by row so a warp's stores spread over all banks) and ships its
     // rows to the peer with one bulk copy, so the slow cluster network never
@@ -674,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (32 * (warp & 3) < Rg) {
+  } else if (warp < 4 && 32 * warp < Rg) {
     // ------------------------------------------------------------------ Q load, softmax, epilogue
     // Waits are polled by one lane per warp and broadcast, so a timeout drains
     // every thread.  A thread owns query row c (TMEM lane c) of the group.
@@ -900,7 +908,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (*abort_s) __nanosleep(100000);
   cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------- fixup
