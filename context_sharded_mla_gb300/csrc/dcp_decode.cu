@@ -298,7 +298,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_q64, const __grid_constant__ CUtensorMap tmap_kv64,
-                      TcArgs a) {
+                      const __grid_constant__ CUtensorMap tmap_kv4, TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -378,6 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmap_kv);
         prefetch_tmap(&tmap_q64);
         prefetch_tmap(&tmap_kv64);
+        prefetch_tmap(&tmap_kv4);
       }
       SegIter it;
       it.init(a.tile_start, U, lo, hi);
@@ -400,20 +401,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       // lane l: page ids of the boxes of tile tile0 + l (-2: not needed, -1: past the table)
       auto fetch_batch = [&](int b, int64_t nvis, int32_t tile0, int32_t tile_end, int32_t (&pg)[8]) {
+        // (local rows and pool rows fit in 32 bits: the host checks the pool size)
         const int32_t tile = tile0 + lane;
-        const int64_t rho0 = (int64_t)tile * kTile;
+        const int32_t rho0 = tile * kTile;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           pg[q] = -2;
-          const int64_t rho = rho0 + (int64_t)q * a.box_rows;
+          const int32_t rho = rho0 + q * a.box_rows;
           if (tile < tile_end && q < nbox && rho < nvis) {
-            const int64_t pidx = rho / a.L.P;
+            const int32_t pidx = rho / a.L.P;
             pg[q] = pidx < a.max_pages ? __ldg(a.bt + (int64_t)b * a.bt_stride + pidx) : -1;
           }
         }
       };
       auto make_boxes = [&](int rs, int32_t tile, const int32_t (&pg)[8], Boxes& bx) {
-        const int64_t rho0 = (int64_t)tile * kTile;
+        const int32_t rho0 = tile * kTile;
+        const int32_t pool0 = rs * (int32_t)a.pool_rows;
         bx.bytes = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -423,8 +426,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (rank == 0 && lane == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
             continue;
           }
-          const int64_t rho = rho0 + (int64_t)q * a.box_rows;
-          bx.y[q] = (int32_t)((int64_t)rs * a.pool_rows + (int64_t)pg[q] * a.L.P + rho % a.L.P);
+          // a box never crosses a page: its height is min(P, 64) and it starts at a
+          // multiple of it, so it starts a page when P <= 64
+          const int32_t rho = rho0 + q * a.box_rows;
+          const int32_t in_page = a.L.P <= kTile ? 0 : rho % a.L.P;
+          bx.y[q] = pool0 + pg[q] * a.L.P + in_page;
           bx.bytes += a.box_rows * 128;
         }
       };
@@ -458,8 +464,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&tfull[ts], bx.bytes * kOwnChunks + bx.bytes / 2);
           unsigned char* dst = ring + ts * kSlotBytes;
-          for (int i = 0; i < kOwnChunks; ++i)
-            issue_chunk(bx, dst + i * kChunkBytes, &tfull[ts], kOwnChunks * (int)rank + i);
+          if (nbox == 1) {
+            // all four value chunks of the tile with one 3-D box: [4 chunks][64 rows][128 B]
+            if (bx.y[0] >= 0) tma_load_3d(dst, &tmap_kv4, &tfull[ts], 0, bx.y[0], kOwnChunks * (int)rank);
+          } else {
+            for (int i = 0; i < kOwnChunks; ++i)
+              issue_chunk(bx, dst + i * kChunkBytes, &tfull[ts], kOwnChunks * (int)rank + i);
+          }
           issue_rope(bx, dst + kRopeOff, &tfull[ts]);
         }
         ++j;
@@ -1106,6 +1117,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // bf16 [rows, 576] row-major, boxes of [box_rows, 64] with 128-byte swizzle, or
 // (half = true) boxes of [box_rows, 32] with 64-byte swizzle
+// bf16 [rows, 576] seen as [9 chunks][rows][64 dims] (dims innermost, then rows,
+// then chunks 128 bytes apart): boxes of [4 chunks][box_rows][64] land as four
+// consecutive 128-byte-swizzled [box_rows][64] tiles.
+bool make_tmap_chunks(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kChunkDims, (cuuint64_t)rows, (cuuint64_t)(kDk / kChunkDims)};
+  cuuint64_t strides[2] = {(cuuint64_t)kDk * 2, (cuuint64_t)kChunkDims * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kChunkDims, box_rows, (cuuint32_t)kOwnChunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool half = false) {
   auto enc = encode_fn();
   if (!enc) return false;
@@ -1162,11 +1188,12 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   if (!workspace || workspace_bytes < p.ws_total) return DCP_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return DCP_ERR_INVALID;
 
-  CUtensorMap tq, tkv, tq64, tkv64;
+  CUtensorMap tq, tkv, tq64, tkv64, tkv4;
   if (!make_tmap(&tq, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg)) return DCP_ERR_CUDA;
   if (!make_tmap(&tkv, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
   if (!make_tmap(&tq64, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg, true)) return DCP_ERR_CUDA;
   if (!make_tmap(&tkv64, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows, true)) return DCP_ERR_CUDA;
+  if (!make_tmap_chunks(&tkv4, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
 
   static size_t smem_set = 0;
   if (smem_set < p.smem) {
@@ -1197,7 +1224,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   cudaStream_t st = as_stream(stream);
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
-  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, a);
+  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, tkv4, a);
   fixup_kernel<<<U, kFixupThreads, 0, st>>>(a);
   return launch_status(3);
 }
