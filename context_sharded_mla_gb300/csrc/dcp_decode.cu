@@ -414,24 +414,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       };
-      auto make_boxes = [&](int rs, int32_t tile, const int32_t (&pg)[8], Boxes& bx) {
-        const int32_t rho0 = tile * kTile;
+      // lane l: pool rows of the boxes of tile tile0 + l from their page ids (-1: no box)
+      auto to_rows = [&](int rs, int32_t tile0, const int32_t (&pg)[8], int32_t (&yb)[8]) {
+        const int32_t rho0 = (tile0 + lane) * kTile;
         const int32_t pool0 = rs * (int32_t)a.pool_rows;
-        bx.bytes = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          bx.y[q] = -1;
+          yb[q] = -1;
           if (pg[q] == -2) continue;
           if (pg[q] < 0 || pg[q] >= a.pool_pages) {
-            if (rank == 0 && lane == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
+            if (rank == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
             continue;
           }
           // a box never crosses a page: its height is min(P, 64) and it starts at a
           // multiple of it, so it starts a page when P <= 64
           const int32_t rho = rho0 + q * a.box_rows;
           const int32_t in_page = a.L.P <= kTile ? 0 : rho % a.L.P;
-          bx.y[q] = pool0 + pg[q] * a.L.P + in_page;
-          bx.bytes += a.box_rows * 128;
+          yb[q] = pool0 + pg[q] * a.L.P + in_page;
+        }
+      };
+      auto make_boxes = [&](const int32_t (&y)[8], Boxes& bx) {
+        bx.bytes = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          bx.y[q] = y[q];
+          if (y[q] >= 0) bx.bytes += a.box_rows * 128;
         }
       };
       // one chunk (all its boxes) into `dst`; exactly as many TMA instructions as
@@ -485,8 +492,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool bad = false;
         const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
         const int32_t t_end = t0 + nt;
-        int32_t pgc[8], pgn[8];
-        fetch_batch(b, nvis, t0, t_end, pgc);
+        // block-table entries of the next 32 tiles are in flight while the
+        // current 32 are issued; each lane turns its tile's entries into TMA rows
+        int32_t pgn[8], yc[8];
+        fetch_batch(b, nvis, t0, t_end, pgn);
+        to_rows(rs, t0, pgn, yc);
         fetch_batch(b, nvis, t0 + 32, t_end, pgn);
         // the query's chunk 4r + 3 and its rope dims [32r, 32r + 32) for the SS part of QK
         if (!warp_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s, lane)) { ok = false; break; }
@@ -501,15 +511,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++seg;
         for (int jj = 0; jj < nt && ok; ++jj) {
           if (jj > 0 && (jj & 31) == 0) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pgc[q] = pgn[q];
+            to_rows(rs, t0 + jj, pgn, yc);
             fetch_batch(b, nvis, t0 + jj + 32, t_end, pgn);
           }
-          int32_t pg[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xffffffffu, pgc[q], jj & 31);
           Boxes cur;
-          make_boxes(rs, t0 + jj, pg, cur);
+          if (nbox == 1) {
+            cur.y[0] = __shfl_sync(0xffffffffu, yc[0], jj & 31);
+            cur.bytes = cur.y[0] >= 0 ? kTile * 128 : 0;
+          } else {
+            int32_t y[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) y[q] = __shfl_sync(0xffffffffu, yc[q], jj & 31);
+            make_boxes(y, cur);
+          }
           ok = load_tile(cur);
         }
       }
