@@ -68,6 +68,7 @@ constexpr int kRopeHalfBytes = kTile * 64;
 constexpr int kRopeOff = kOwnChunks * kChunkBytes;         // rope part inside a tile slot
 constexpr int kSlotBytes = kRopeOff + kRopeHalfBytes;      // 36 KB per tile slot
 constexpr int kMaxTileSlots = 8;
+constexpr int kL2Ahead = 2;                   // tiles between a tile's L2 prefetch and its ring load
 constexpr int kFixedBarSlots = 32;            // mbarriers other than the per-slot ones
 constexpr int kThreads = 384;                 // 12 warps (roles below)
 // Warp roles.  Warp w runs on SM sub-partition w % 4 and reaches TMEM lanes
@@ -433,6 +434,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           yb[q] = pool0 + pg[q] * a.L.P + in_page;
         }
       };
+      // the same rows without the bad-page report (the batch is checked again when it is issued)
+      auto to_rows_quiet = [&](int rs, int32_t tile0, const int32_t (&pg)[8], int32_t (&yb)[8]) {
+        const int32_t rho0 = (tile0 + lane) * kTile;
+        const int32_t pool0 = rs * (int32_t)a.pool_rows;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int32_t rho = rho0 + q * a.box_rows;
+          yb[q] = (pg[q] < 0 || pg[q] >= a.pool_pages) ? -1 : pool0 + pg[q] * a.L.P + (a.L.P <= kTile ? 0 : rho % a.L.P);
+        }
+      };
       auto make_boxes = [&](const int32_t (&y)[8], Boxes& bx) {
         bx.bytes = 0;
 #pragma unroll
@@ -494,7 +505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t t_end = t0 + nt;
         // block-table entries of the next 32 tiles are in flight while the
         // current 32 are issued; each lane turns its tile's entries into TMA rows
-        int32_t pgn[8], yc[8];
+        int32_t pgn[8], yc[8], yn = -1;  // yn: next batch's first-box rows (L2 prefetch)
         fetch_batch(b, nvis, t0, t_end, pgn);
         to_rows(rs, t0, pgn, yc);
         fetch_batch(b, nvis, t0 + 32, t_end, pgn);
@@ -513,6 +524,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (jj > 0 && (jj & 31) == 0) {
             to_rows(rs, t0 + jj, pgn, yc);
             fetch_batch(b, nvis, t0 + jj + 32, t_end, pgn);
+          }
+          if (nbox == 1) {
+            // The ring holds a few tiles, fewer than HBM latency times the tile
+            // rate: each tile is also prefetched into L2 kL2Ahead tiles before its
+            // ring load, so that the load finds it there.
+            // The next batch's rows, once its block-table entries have arrived:
+            if ((jj & 31) == 32 - kL2Ahead) {
+              int32_t yt[8];
+              to_rows_quiet(rs, t0 + jj + kL2Ahead, pgn, yt);
+              yn = yt[0];
+            }
+            // tile jj + kL2Ahead into L2, so that its ring load finds it there
+            const int32_t ja = jj + kL2Ahead;
+            const int32_t ya = __shfl_sync(0xffffffffu, (ja & 31) > (jj & 31) ? yc[0] : yn, ja & 31);
+            if (lane == 0 && ja < nt && ya >= 0) {
+              tma_prefetch_3d(&tmap_kv4, 0, ya, kOwnChunks * (int)rank);
+              tma_prefetch_2d(&tmap_kv64, 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, ya);
+            }
           }
           Boxes cur;
           if (nbox == 1) {
