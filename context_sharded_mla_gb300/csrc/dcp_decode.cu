@@ -270,22 +270,21 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Warp-uniform bounded waits: lane 0 polls and broadcasts; on success every lane
-// tests the completed phase once more, which gives each lane its own acquire.
+// Warp-uniform bounded waits.  Fast path: every lane tests the phase once (its
+// own acquire) and one vote confirms; otherwise each lane waits with the bounded
+// loop and a final vote makes the outcome uniform (false after an abort).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_s, int lane) {
-  int r = 1;
-  if (lane == 0) r = mbar_wait(bar, parity, abort_s) ? 1 : 0;
-  r = __shfl_sync(0xffffffffu, r, 0);
-  if (r) mbar_try_wait(bar, parity);
-  return r != 0;
+  bool ok = mbar_try_wait(bar, parity);  // every lane: its own acquire
+  if (__all_sync(0xffffffffu, ok)) return true;
+  if (!ok) ok = mbar_wait(bar, parity, abort_s);
+  return __all_sync(0xffffffffu, ok);  // warp-uniform (false after an abort)
 }
 
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_s, int lane) {
-  int r = 1;
-  if (lane == 0) r = mbar_wait_cluster(bar, parity, abort_s) ? 1 : 0;
-  r = __shfl_sync(0xffffffffu, r, 0);
-  if (r) mbar_try_wait_cluster(bar, parity);
-  return r != 0;
+  bool ok = mbar_try_wait_cluster(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  if (!ok) ok = mbar_wait_cluster(bar, parity, abort_s);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------------------- main kernel
