@@ -76,7 +76,7 @@ constexpr int kThreads = 384;                 // 12 warps (roles below)
 // are q and 4 + q.  The tensor-core issuer (a polling thread) sits with the
 // warps of quarter 3, the quarter a group of up to 96 rows leaves empty, and
 // the producer with quarter 2; warps 8 and 9 have no role.
-constexpr int kSenderWarp0 = 4;
+constexpr int kHalfRows = 16;                 // rows served by one softmax warp (two threads per row)
 constexpr int kProducerWarp = 10;
 constexpr int kMmaWarp = 11;
 constexpr int kMaxGroupRows = 128;
@@ -137,8 +137,7 @@ __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
 }
 
 enum Bar { kQFull = 0, kQEmpty, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kOFree,
-           kXFull = 11,  // [2 buffers][4 row quarters]: the peer's rows of a quarter have landed
-           kXRead = 19,  // [2 buffers][4 row quarters]: my softmax warp of the quarter has read them
+           kXFull = 11,  // [2 buffers][8 channels]: the peer's partial scores of a channel's rows have landed
            kNumFixedBars = 27 };
 static_assert(kNumFixedBars <= kFixedBarSlots, "fixed barriers");
 
@@ -287,6 +286,56 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return __all_sync(0xffffffffu, ok);
 }
 
+// O rows of one softmax warp scaled by f (16 lanes from `o_addr`'s lane;
+// thread t: row t % 16, columns [128 (t / 16), 128 (t / 16) + 128)).
+__device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
+#pragma unroll 1
+  for (int k = 0; k < 4; ++k) {
+    uint32_t r[32];
+    tmem_ld16x2<128>(o_addr + 32 * k, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+    tmem_st16x2<128>(o_addr + 32 * k, r);
+  }
+  tmem_st_wait();
+}
+
+// The same O rows times `inv` -> the output row (bf16 or fp32) or the fp32
+// piece row; thread t writes dims [d0, d0 + 128) of its row.
+__device__ __forceinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, bool writes, bool whole,
+                                             int64_t out_row, int64_t piece_row, int d0, float inv) {
+#pragma unroll 1
+  for (int k = 0; k < 4; ++k) {
+    uint32_t rr[32];
+    tmem_ld16x2<128>(o_addr + 32 * k, rr);
+    tmem_ld_wait();
+    if (!writes) continue;
+    const int d = d0 + 32 * k;
+    if (whole && a.o_bf16) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[8 * i + 2 * e]) * inv,
+                                                    __uint_as_float(rr[8 * i + 2 * e + 1]) * inv);
+          w[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      float* base = whole ? static_cast<float*>(a.o_part) + out_row * kDv + d : a.piece_o + piece_row * kDv + d;
+      float4* dst = reinterpret_cast<float4*>(base);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(rr[4 * i]) * inv, __uint_as_float(rr[4 * i + 1]) * inv,
+                             __uint_as_float(rr[4 * i + 2]) * inv, __uint_as_float(rr[4 * i + 3]) * inv);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------- main kernel
 // A 2-CTA cluster per (work range, row group).  CTA `rank` loads key/value dims
 // [256 rank, 256 rank + 256) of every tile (CTA 0 also the 64 rope dims),
@@ -322,7 +371,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int g = cid % a.ngroups;
   const int Rg = a.Rg;
   const int nts = a.nts;
-  const int nact = (Rg + 31) >> 5;  // softmax warps holding at least one row of the group
+  int nhalf = 0;  // softmax warps with rows of the group (warp w < 8 serves rows 32 (w % 4) + 16 (w / 4) + [0, 16))
+  for (int w = 0; w < 8; ++w) nhalf += 32 * (w & 3) + kHalfRows * (w >> 2) < Rg;
   const int32_t U = a.B * a.n_held;
   const int64_t T = a.tile_start[U];
   const int64_t lo = range_lo(T, v, a.V), hi = range_lo(T, v + 1, a.V);
@@ -331,17 +381,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     *abort_s = 0;
     for (int i = 0; i < kNumFixedBars; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&bars[kQFull], nact + 1);  // softmax warps + the query-chunk TMA
-    mbar_init(&bars[kSFree0], 2 * nact);  // sender and softmax warps have read the partial scores
-    mbar_init(&bars[kSFree1], 2 * nact);
-    mbar_init(&bars[kPFull0], nact);
-    mbar_init(&bars[kPFull1], nact);
-    mbar_init(&bars[kOFree], nact);
-    // The score exchange runs as one channel per row quarter (a sender warp ships
-    // the rows of its TMEM lane quarter and the softmax warp of that quarter reads
-    // them): one "landed" and one "read" barrier per buffer and quarter, so no
-    // barrier can run two phases ahead of its waiter (all are single-arrival).
-
+    mbar_init(&bars[kQFull], nhalf + 1);  // softmax warps + the query-chunk TMA
+    mbar_init(&bars[kSFree0], nhalf);     // every softmax warp has read the partial scores
+    mbar_init(&bars[kSFree1], nhalf);
+    mbar_init(&bars[kPFull0], nhalf);
+    mbar_init(&bars[kPFull1], nhalf);
+    mbar_init(&bars[kOFree], nhalf);
+    // The score exchange runs as one channel per softmax warp (its 16 rows), with
+    // one single-arrival "landed" barrier per buffer and channel.
     for (int i = 0; i < nts; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 1);
@@ -349,8 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     // tile j's partial scores from the peer land in buffer (j & 1) ^ 1: expect tiles 0 and 1
     for (uint32_t j = 0; j < 2 && j < ntiles_cta; ++j)
-      for (int q = 0; q < nact; ++q)
-        mbar_arrive_expect_tx(&bars[kXFull + 4 * ((j & 1) ^ 1) + q], (uint32_t)min(32, Rg - 32 * q) * kXRowBytes);
+      for (int w = 0; w < 8; ++w)
+        if (32 * (w & 3) + kHalfRows * (w >> 2) < Rg)
+          mbar_arrive_expect_tx(&bars[kXFull + 8 * ((j & 1) ^ 1) + w], kHalfRows * kXRowBytes);
   }
   // rows of a page past a request's length are read with zero weight: start from finite zeros
   for (int i = tid; i < nts * kSlotBytes / 16; i += kThreads) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
@@ -682,71 +730,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kSenderWarp0 && warp < kSenderWarp0 + 4) {
-    // ------------------------------------------------------------------ score senders
-    // Warp 4 + q reads TMEM lanes [32 q, 32 q + 32) of each tile's partial
-    // scores, stages them in shared memory (256-byte rows, 16-byte pieces
-    // swizzled by row so a warp's stores spread over all banks) and ships its
-    // rows to the peer with one bulk copy, so the slow cluster network never
-    // holds up the shared-memory pipe the softmax warps read through.  Two buffers per CTA swap roles every tile:
-    // tile j is staged in buffer j & 1 and the peer's tile j lands in buffer
-    // (j & 1) ^ 1.  Both conditions for tile j are local: my buffer j & 1 held
-    // the peer's tile j - 1, which my softmax warps have read; the peer's buffer
-    // (j & 1) ^ 1 held its staged tile j - 1, whose copy to me has landed (it
-    // was read here).
-    const int c = 32 * (warp & 3) + lane;
-    if (32 * (warp & 3) < Rg && lo < hi) {
-      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-      const bool has_x = c < Rg;
-      const uint32_t peer = rank ^ 1u;
-      const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer);
-      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull + (warp & 3)]), peer);
-      for (uint32_t j = 0; j < ntiles_cta; ++j) {
-        uint32_t s[64];
-        if (!warp_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_s, lane)) break;
-        tc_fence_after();
-        const uint32_t sa = tmem + lane_base + kSCol + kTile * (j & 1);
-        tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
-        // my softmax warps have read the peer's tile j - 1 out of buffer j & 1
-        const uint32_t sb = j & 1;
-        if (j > 0 && !warp_wait(&bars[kXRead + 4 * sb + (warp & 3)], ((j - 1) >> 1) & 1, abort_s, lane)) break;
-        unsigned char* stage = x_s + sb * sl.xbuf;
-        if (has_x) {
-          const uint32_t stage_row = smem_u32(stage) + (uint32_t)c * kXRowBytes;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            st_shared_v4(stage_row + ((uint32_t)(i ^ (c & 15)) << 4), s[4 * i], s[4 * i + 1], s[4 * i + 2],
-                         s[4 * i + 3]);
-        }
-        fence_proxy_async_smem();  // the copy engine reads the staged rows
-        __syncwarp();
-        if (lane == 0) {
-          // this warp's rows [32 q, 32 q + rows) go out as one copy; the peer's
-          // barrier expects the bytes of all the warps' copies
-          const uint32_t r0 = 32 * (warp & 3);
-          const uint32_t rows = min(32, Rg - (int)r0);
-          bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf + r0 * kXRowBytes, stage + r0 * kXRowBytes,
-                            rows * kXRowBytes, xfull_peer + 8 * 4 * (sb ^ 1));
-        }
-      }
-    }
-  } else if (warp < 4 && 32 * warp < Rg) {
-    // ------------------------------------------------------------------ Q load, softmax, epilogue
-    // Waits are polled by one lane per warp and broadcast, so a timeout drains
-    // every thread.  A thread owns query row c (TMEM lane c) of the group.
-    const int c = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const bool has_x = c < Rg;  // this row's partial scores cross between the CTAs
-    const uint32_t x_mine = smem_u32(x_s) + (uint32_t)c * kXRowBytes;
+  } else if (warp < 8 && 32 * (warp & 3) + kHalfRows * (warp >> 2) < Rg) {
+    // ------------------------------------------------------------------ score exchange, softmax, epilogue
+    // Warp w < 8 serves the 16 rows [r0, r0 + 16), r0 = 32 (w % 4) + 16 (w / 4),
+    // with two threads per row: thread t takes row r0 + t % 16 and keys
+    // [32 (t / 16), 32 (t / 16) + 32) of each tile (O columns [128 (t / 16), +128)).
+    // Per tile j it reads its rows of this CTA's partial scores S_j^r, adds the
+    // peer's (landed in buffer (j & 1) ^ 1) and runs the online softmax.  It also
+    // ships its rows of S_j^r to the peer: staged in buffer j & 1 and sent with
+    // one bulk copy, as soon as that buffer is free -- right after this warp has
+    // read the peer's tile j - 1 out of it (my copy of tile j - 1 out of the
+    // peer's buffer had landed by then), if S_j is ready, else at the start of
+    // tile j.  Both conditions are local, so no barrier guards the buffers.
+    // Waits are warp-wide and bounded, so a timeout drains every thread.
+    const int r0 = 32 * (warp & 3) + kHalfRows * (warp >> 2);
+    const int ch = warp;  // exchange channel
+    const int h = lane >> 4;
+    const int row = r0 + (lane & 15);
+    const uint32_t lane_addr = (uint32_t)r0 << 16;
+    const uint32_t xrow = (uint32_t)row * kXRowBytes;
     if (lo < hi) {
       auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_s, lane); };
       auto wwait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
         return warp_wait_cluster(bar, parity, abort_s, lane);
+      };
+      const uint32_t peer = rank ^ 1u;
+      const uint32_t x_peer = mapa_shared(smem_u32(x_s), peer);
+      const uint32_t xfull_peer = mapa_shared(smem_u32(&bars[kXFull + ch]), peer);
+      // this warp's rows of S_js (in registers) -> buffer js & 1 -> the peer's buffer (js & 1) ^ 1
+      auto send = [&](uint32_t js, const uint32_t (&sv)[32]) {
+        const uint32_t sb = js & 1;
+        const uint32_t dst = smem_u32(x_s) + sb * sl.xbuf + xrow;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(dst + ((uint32_t)((8 * h + i) ^ (row & 15)) << 4), sv[4 * i], sv[4 * i + 1], sv[4 * i + 2],
+                       sv[4 * i + 3]);
+        fence_proxy_async_smem();  // the copy engine reads the staged rows
+        __syncwarp();
+        if (lane == 0)
+          bulk_copy_to_peer(x_peer + (sb ^ 1) * sl.xbuf + (uint32_t)r0 * kXRowBytes,
+                            x_s + sb * sl.xbuf + (uint32_t)r0 * kXRowBytes, kHalfRows * kXRowBytes,
+                            xfull_peer + 8 * 8 * (sb ^ 1));
       };
       SegIter it;
       it.init(a.tile_start, U, lo, hi);
@@ -755,90 +779,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t jglob = 0;
       int seg = 0;
       bool ok = true;
+      bool sent = false;  // this warp's rows of S_jglob have been shipped already
       while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
         const int b = u / a.n_held, rs = u % a.n_held;
         const int64_t S = a.seq_lens[b];
-        const int grow = g * Rg + c;
-        const bool active = c < Rg && grow < a.R_total && S >= a.q_len;
-        int64_t nvis = 0;
-        if (active) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
-        // ---- this CTA's first 192 c_K dims of the row -> TMEM lane c, columns [416, 512)
+        const int grow = g * Rg + row;
+        int64_t nvis = 0;  // keys of this shard visible to the row
+        if (row < Rg && grow < a.R_total && S >= a.q_len)
+          nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
+        // ---- query chunks 4r, 4r + 1 of the rows -> TMEM (thread t: chunk t / 16 of its row)
         if (!wwait(&bars[kQEmpty], (seg & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         {
-          const bool has_row = c < Rg && grow < a.R_total;
-          const uint4* src =
-              reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk + 256 * (int)rank);
-#pragma unroll 1
-          for (int i = 0; i < kQTmemChunks; ++i) {
-            uint32_t r[32];
+          const bool has_row = row < Rg && grow < a.R_total;
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk +
+                                                            256 * (int)rank + kChunkDims * h);
+          uint32_t r[32];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              uint4 w4 = has_row ? __ldg(src + 8 * i + k) : make_uint4(0, 0, 0, 0);
-              r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
-            }
-            tmem_st32(tmem + lane_base + kQCol + 32 * i, r);
+          for (int k = 0; k < 8; ++k) {
+            uint4 w4 = has_row ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+            r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
           }
+          tmem_st16x2<32>(tmem + lane_addr + kQCol, r);
           tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kQFull]);
         ++seg;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY;  // running maximum of the row (log2 units)
+        float l = 0.f;            // this thread's half of the row's running sum
+        float l_row = 0.f;        // the row's running sum
         for (int jj = 0; jj < nt; ++jj, ++jglob) {
-          const uint32_t j = jglob;
+          const uint32_t j = jglob, bsel = j & 1, rb = bsel ^ 1;
           // ---- this CTA's partial scores of tile j
-          uint32_t s[64];  // score bits
-          if (!wwait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+          uint32_t s[32];  // score bits, keys [32 h, 32 h + 32)
+          if (!wwait(&bars[kSFull0 + bsel], (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          {
-            const uint32_t sa = tmem + lane_base + kSCol + kTile * (j & 1);
-            tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_ld_wait();
-          }
+          tmem_ld16x2<32>(tmem + lane_addr + kSCol + kTile * bsel, s);
+          tmem_ld_wait();
+          if (!sent) send(j, s);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kSFree0 + (j & 1)]);
+          if (lane == 0) mbar_arrive(&bars[kSFree0 + bsel]);
           // ---- the peer's partial scores of tile j: S = mine + peer's
-          const uint32_t rb = (j & 1) ^ 1;  // receive buffer of tile j
-          if (!wwait_cluster(&bars[kXFull + 4 * rb + (warp & 3)], (j >> 1) & 1)) { ok = false; break; }
-          if (has_x) {
-            const uint32_t src = x_mine + rb * sl.xbuf;
+          if (!wwait_cluster(&bars[kXFull + 8 * rb + ch], (j >> 1) & 1)) { ok = false; break; }
+          {
+            const uint32_t src = smem_u32(x_s) + rb * sl.xbuf + xrow;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const uint4 w4 = ld_shared_v4(src + ((uint32_t)(i ^ (c & 15)) << 4));
+            for (int i = 0; i < 8; ++i) {
+              const uint4 w4 = ld_shared_v4(src + ((uint32_t)((8 * h + i) ^ (row & 15)) << 4));
               const uint64_t a0 = f2_add(f2_pack(s[4 * i], s[4 * i + 1]), f2_pack(w4.x, w4.y));
               const uint64_t a1 = f2_add(f2_pack(s[4 * i + 2], s[4 * i + 3]), f2_pack(w4.z, w4.w));
               f2_unpack(a0, s[4 * i], s[4 * i + 1]);
               f2_unpack(a1, s[4 * i + 2], s[4 * i + 3]);
             }
           }
-          // The adds above consumed every lane's reads: the buffer may be restaged.
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars[kXRead + 4 * rb + (warp & 3)]);
-            // the next phase of this buffer's quarter expects the peer's tile j + 2
-            if (j + 2 < ntiles_cta)
-              mbar_arrive_expect_tx(&bars[kXFull + 4 * rb + (warp & 3)],
-                                    (uint32_t)min(32, Rg - 32 * (warp & 3)) * kXRowBytes);
+          __syncwarp();  // every lane's reads of buffer rb are done
+          if (lane == 0 && j + 2 < ntiles_cta)
+            mbar_arrive_expect_tx(&bars[kXFull + 8 * rb + ch], kHalfRows * kXRowBytes);
+          // ---- buffer rb is free: ship S_{j+1} now if the product is done
+          sent = false;
+          if (j + 1 < ntiles_cta && __all_sync(0xffffffffu, mbar_test(&bars[kSFull0 + rb], ((j + 1) >> 1) & 1))) {
+            uint32_t s2[32];
+            tc_fence_after();
+            tmem_ld16x2<32>(tmem + lane_addr + kSCol + kTile * rb, s2);
+            tmem_ld_wait();
+            send(j + 1, s2);
+            sent = true;
           }
           // ---- online softmax of tile j
-          const int64_t rho0 = (int64_t)(t0 + jj) * kTile;
-          const int64_t lim = nvis - rho0;  // columns k < lim are visible to this row
-          if (lim < kTile) {
+          const int64_t lim = nvis - ((int64_t)(t0 + jj) * kTile + 32 * h);  // keys k < lim are visible
+          if (lim < 32) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
+            for (int k = 0; k < 32; ++k)
               if (k >= lim) s[k] = __float_as_uint(-INFINITY);
           }
-          float mx[8];
+          float mx[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(s[k]);
+          for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(s[k]);
 #pragma unroll
-          for (int k = 8; k < 64; k += 2)
-            mx[((k - 8) >> 1) & 7] = fmax3(mx[((k - 8) >> 1) & 7], __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
-          const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          for (int k = 4; k < 32; k += 2)
+            mx[((k - 4) >> 1) & 3] = fmax3(mx[((k - 4) >> 1) & 3], __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
+          float mraw = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+          mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));  // the row's other 32 keys
           const float mt = mraw * a.scale_log2;  // scale > 0: the max commutes with the scaling
           bool need = false;
           float alpha = 1.f;
@@ -849,97 +873,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             alpha = exp2f(m_ref - mt);
             m_ref = mt;
           }
-          if (__any_sync(0xffffffffu, need && has_x)) {
+          if (__any_sync(0xffffffffu, need)) {
             // rows whose maximum moved: scale their O row once PV(j - 1) is done
             // (a row's maximum is finite only after a tile of this segment, so j >= 1)
             if (!wwait(&bars[kPVDone0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 8; ++q) {
-              uint32_t r[32];
-              const uint32_t addr = tmem + lane_base + kOCol + 32 * q;
-              tmem_ld32(addr, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(addr, r);
-            }
-            tmem_st_wait();
-            l *= alpha;
+            rescale_rows(tmem + lane_addr + kOCol, alpha);
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           const float cs = a.scale_log2;
           const uint64_t cs2 = f2_pack(__float_as_uint(cs), __float_as_uint(cs));
           const uint64_t nm2 = f2_pack(__float_as_uint(-m_use), __float_as_uint(-m_use));
           uint64_t ps[4] = {0, 0, 0, 0};  // pairs of partial row sums (+0.f bits)
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < 16; ++k) {
             uint32_t x0, x1;
             f2_unpack(f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), cs2, nm2), x0, x1);
             const float p0 = fast_exp2(__uint_as_float(x0));
             const float p1 = fast_exp2(__uint_as_float(x1));
             ps[k & 3] = f2_add(ps[k & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            pk[k] = *reinterpret_cast<uint32_t*>(&h);
+            __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&hh);
           }
           {
             uint32_t a0, a1;
             f2_unpack(f2_add(f2_add(ps[0], ps[1]), f2_add(ps[2], ps[3])), a0, a1);
-            l += __uint_as_float(a0) + __uint_as_float(a1);
+            l = l * alpha + (__uint_as_float(a0) + __uint_as_float(a1));
           }
-          // P(j) -> TMEM (A operand of the PV product) once PV(j - 2) has read
-          // the buffer's previous contents
-          if (j >= 2 && !wwait(&bars[kPVDone0 + (j & 1)], ((j - 2) >> 1) & 1)) { ok = false; break; }
+          // P(j) -> TMEM (A operand of the PV product) once PV(j - 2) has read the buffer
+          if (j >= 2 && !wwait(&bars[kPVDone0 + bsel], ((j - 2) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          tmem_st32(tmem + lane_base + kPCol + 32 * (j & 1), pk);
+          tmem_st16x2_16<16>(tmem + lane_addr + kPCol + 32 * bsel, pk);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
+          if (lane == 0) mbar_arrive(&bars[kPFull0 + bsel]);
         }
         if (!ok) break;
-        // ---------------- epilogue: O row / l -> o (this CTA's 256 dims), lse
+        l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+        // ---------------- epilogue: O rows / l -> o (this CTA's 256 dims), lse
         const uint32_t jl = jglob - 1;
         if (!wwait(&bars[kPVDone0 + (jl & 1)], (jl >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-        const int R_here = min(Rg, a.R_total - g * Rg);
-        const bool writes = c < R_here;
-        const int64_t out_row = ((int64_t)rs * a.B + b) * a.R_total + g * Rg + c;
-        const int64_t piece_row = (int64_t)(2 * v + kslot) * a.R_total + g * Rg + c;
-#pragma unroll 1
-        for (int q = 0; q < 8; ++q) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kOCol + 32 * q, r);
-          tmem_ld_wait();
-          if (writes) {
-            const int d0 = 256 * (int)rank + 32 * q;
-            if (whole && a.o_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d0);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
-                                                           __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
-                  w[e] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-              float* base = whole ? static_cast<float*>(a.o_part) + out_row * kDv + d0 : a.piece_o + piece_row * kDv + d0;
-              float4* dst = reinterpret_cast<float4*>(base);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                     __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-            }
-          }
-        }
-        if (writes && rank == 0) {
+        const bool writes = row < min(Rg, a.R_total - g * Rg);
+        const int64_t out_row = ((int64_t)rs * a.B + b) * a.R_total + g * Rg + row;
+        const int64_t piece_row = (int64_t)(2 * v + kslot) * a.R_total + g * Rg + row;
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        store_o_rows(a, tmem + lane_addr + kOCol, writes, whole, out_row, piece_row, 256 * (int)rank + 128 * h, inv);
+        if (writes && h == 0 && rank == 0) {
+          const float lse2 = l_row > 0.f ? m_ref + log2f(l_row) : -INFINITY;
           if (whole)
             a.lse_part[out_row] = a.base2 ? lse2 : lse2 * kLn2;
           else
