@@ -78,7 +78,8 @@ constexpr int kThreads = 384;                 // 12 warps (roles below)
 // the producer with quarter 2; warps 8 and 9 have no role.
 constexpr int kHalfRows = 16;                 // rows served by one softmax warp (two threads per row)
 constexpr int kProducerWarp = 10;
-constexpr int kMmaWarp = 11;
+constexpr int kMmaWarp = 11;                  // QK issuer and TMEM owner
+constexpr int kPvWarp = 9;                    // PV issuer
 constexpr int kMaxGroupRows = 128;
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
 constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns
@@ -613,21 +614,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Event-driven single thread: QK(j) once tile j has landed and the S tile it
-    // writes (last used by tile j - 2) has been read; PV(j) once P(j) is ready.
+    // ------------------------------------------------------------------ QK issuer
     if (lane == 0 && lo < hi) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t kdesc0 = sw128_desc(smem_u32(ring), 16, 1024);
-      const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
       const uint64_t qcdesc0 = sw128_desc(smem_u32(qc_s), 16, 1024);
       const uint64_t qrdesc0 = sw64_desc(smem_u32(qr_s), 512);
       const uint64_t rdesc0 = sw64_desc(smem_u32(ring + kRopeOff), 512);
-      // QK(j): query chunks 4r .. 4r + 2 from TMEM (12 MMAs), chunk 4r + 3 and the
-      // rope half from shared memory (4 + 2 MMAs), back to back.  (Issuing the
-      // product in pieces with PV products slipped in between was measured
-      // slower: it delays the scores that the exchange is waiting for.)
+      // QK(j): query chunks 4r, 4r + 1 from TMEM (8 MMAs), chunks 4r + 2, 4r + 3
+      // and the rope half from shared memory (8 + 2 MMAs), back to back.
       auto issue_qk = [&](uint32_t j, uint32_t ts) {
         const uint32_t d = tmem + kSCol + kTile * (j & 1);
         const uint32_t soff = (ts * kSlotBytes) >> 4;
@@ -648,86 +643,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kRopeHalf / 16; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rdesc0 + soff + 2 * kk, idesc_qk, 1);
         mma_commit(&bars[kSFull0 + (j & 1)]);
       };
-      auto issue_pv = [&](uint32_t j, uint32_t ts, bool first) {
-        const uint32_t pa = tmem + kPCol + 32 * (j & 1);  // P(j): 64 bf16 = 32 columns
-        const uint64_t vd = vdesc0 + ((ts * kSlotBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + kOCol, pa + 8 * kk, vd + kk * (2048 >> 4), idesc_pv, !(first && kk == 0));
-        mma_commit(&tempty[ts]);
-        mma_commit(&bars[kPVDone0 + (j & 1)]);
-      };
-      uint32_t ts_q = 0, ph_q = 0, ts_p = 0;  // ring slots of the next QK and PV products
+      // Two issuing threads, each blocking in order on its own conditions (no
+      // polling loop): lane 0 of this warp issues QK(j) once tile j has landed
+      // and the S tile it writes (last used by tile j - 2) has been read; lane 0
+      // of warp kPvWarp issues PV(j) once P(j) is ready.  Both feed the same
+      // in-order tensor pipe; each commit tracks its own thread's products.
+      uint32_t ts_q = 0, ph_q = 0;  // ring slot of the next QK product and its use parity
       SegIter itq;
       itq.init(a.tile_start, U, lo, hi);
       int32_t uq, t0q, ntq, ksq;
       bool wq;
-      bool q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
-      int q_seg = 0, q_jj = 0;
-      bool q_seg_ready = false;
       uint32_t jq = 0;
+      int q_seg = 0;
+      bool ok = true;
+      while (ok && itq.next(&uq, &t0q, &ntq, &wq, &ksq)) {
+        for (int q_jj = 0; q_jj < ntq; ++q_jj, ++jq) {
+          if (!mbar_wait(&bars[kSFree0 + (jq & 1)], ((jq >> 1) & 1) ^ 1, abort_s) ||
+              (q_jj == 0 && !mbar_wait(&bars[kQFull], q_seg & 1, abort_s)) || !mbar_wait(&tfull[ts_q], ph_q, abort_s)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(jq, ts_q);
+          if (++ts_q == (uint32_t)nts) {
+            ts_q = 0;
+            ph_q ^= 1;
+          }
+          if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
+        }
+        ++q_seg;
+      }
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0 && lo < hi) {
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, 0, 1);
+      const uint64_t vdesc0 = sw128_desc(smem_u32(ring), kChunkBytes, 1024);
       SegIter itp;
       itp.init(a.tile_start, U, lo, hi);
       int32_t up, t0p, ntp, ksp;
       bool wp;
-      bool p_has = itp.next(&up, &t0p, &ntp, &wp, &ksp);
-      int p_seg = 0, p_jj = 0;
-      uint32_t jp = 0;
-      uint64_t idle_since = 0;
-      uint32_t idle_polls = 0;
-      while (q_has || p_has) {
-        bool progress = false;
-        if (p_has && jp < jq) {
-          bool ready = mbar_test(&bars[kPFull0 + (jp & 1)], (jp >> 1) & 1);
-          if (ready && p_jj == 0 && p_seg >= 1) ready = mbar_test(&bars[kOFree], (p_seg - 1) & 1);
-          if (ready) {
-            tc_fence_after();
-            issue_pv(jp, ts_p, p_jj == 0);
-            if (++ts_p == (uint32_t)nts) ts_p = 0;
-            ++jp;
-            if (++p_jj == ntp) {
-              ++p_seg;
-              p_jj = 0;
-              p_has = itp.next(&up, &t0p, &ntp, &wp, &ksp);
-            }
-            progress = true;
-          }
-        }
-        // the S tile of jq was last used by tile jq - 2: both its readers must be
-        // done before QK(jq) starts; the whole product goes out back to back
-        if (q_has && mbar_test(&bars[kSFree0 + (jq & 1)], ((jq >> 1) & 1) ^ 1)) {
-          if (!q_seg_ready && mbar_test(&bars[kQFull], q_seg & 1)) q_seg_ready = true;
-          if (q_seg_ready && mbar_test(&tfull[ts_q], ph_q)) {
-            tc_fence_after();
-            issue_qk(jq, ts_q);
-            if (++ts_q == (uint32_t)nts) {
-              ts_q = 0;
-              ph_q ^= 1;
-            }
-            if (q_jj == ntq - 1) mma_commit(&bars[kQEmpty]);
-            ++jq;
-            if (++q_jj == ntq) {
-              ++q_seg;
-              q_jj = 0;
-              q_seg_ready = false;
-              q_has = itq.next(&uq, &t0q, &ntq, &wq, &ksq);
-            }
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_since = 0;
-          idle_polls = 0;
-        } else if ((++idle_polls & 31) == 0) {  // look at the clock every 32 idle polls
-          if (*abort_s) break;
-          const uint64_t now = globaltimer();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (now - idle_since > kWaitLimitNs) {
-            *abort_s = 1;
+      uint32_t jp = 0, ts_p = 0;
+      int p_seg = 0;
+      bool ok = true;
+      while (ok && itp.next(&up, &t0p, &ntp, &wp, &ksp)) {
+        for (int p_jj = 0; p_jj < ntp; ++p_jj, ++jp) {
+          // P(j) ready; the first product of a segment also needs the previous
+          // segment's O read out
+          if (!mbar_wait(&bars[kPFull0 + (jp & 1)], (jp >> 1) & 1, abort_s) ||
+              (p_jj == 0 && p_seg >= 1 && !mbar_wait(&bars[kOFree], (p_seg - 1) & 1, abort_s))) {
+            ok = false;
             break;
           }
+          tc_fence_after();
+          const uint32_t pa = tmem + kPCol + 32 * (jp & 1);  // P(j): 64 bf16 = 32 columns
+          const uint64_t vd = vdesc0 + ((ts_p * kSlotBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + kOCol, pa + 8 * kk, vd + kk * (2048 >> 4), idesc_pv, !(p_jj == 0 && kk == 0));
+          mma_commit(&tempty[ts_p]);
+          mma_commit(&bars[kPVDone0 + (jp & 1)]);
+          if (++ts_p == (uint32_t)nts) ts_p = 0;
         }
+        ++p_seg;
       }
     }
   } else if (warp < 8 && 32 * (warp & 3) + kHalfRows * (warp >> 2) < Rg) {
