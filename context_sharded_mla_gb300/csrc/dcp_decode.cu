@@ -303,9 +303,13 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
 }
 
 // The same O rows times `inv` -> the output row (bf16 or fp32) or the fp32
-// piece row; thread t writes dims [d0, d0 + 128) of its row.
-__device__ __forceinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, bool writes, bool whole,
+// piece row; thread t writes dims [d0, d0 + 128) of its row.  Each lane's
+// stores go to a different row, so they are made as wide as the alignment
+// allows (32 bytes: whole sectors, half the store instructions).  Kept out of
+// line: it runs once per segment and inlining it cost the tile loop.
+__device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, bool writes, bool whole,
                                              int64_t out_row, int64_t piece_row, int d0, float inv) {
+  const bool wide = (reinterpret_cast<uintptr_t>(a.o_part) & 31) == 0;  // pieces are 256-byte aligned
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
     uint32_t rr[32];
@@ -314,25 +318,35 @@ __device__ __forceinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, b
     if (!writes) continue;
     const int d = d0 + 32 * k;
     if (whole && a.o_bf16) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d);
+      uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t w[4];
+      for (int e = 0; e < 16; ++e) {
+        __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
+        w[e] = *reinterpret_cast<uint32_t*>(&hh);
+      }
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d;
+      if (wide) {
+        st_global_v8(dst, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+        st_global_v8(dst + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+      } else {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[8 * i + 2 * e]) * inv,
-                                                    __uint_as_float(rr[8 * i + 2 * e + 1]) * inv);
-          w[e] = *reinterpret_cast<uint32_t*>(&hh);
-        }
-        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     } else {
       float* base = whole ? static_cast<float*>(a.o_part) + out_row * kDv + d : a.piece_o + piece_row * kDv + d;
-      float4* dst = reinterpret_cast<float4*>(base);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = make_float4(__uint_as_float(rr[4 * i]) * inv, __uint_as_float(rr[4 * i + 1]) * inv,
-                             __uint_as_float(rr[4 * i + 2]) * inv, __uint_as_float(rr[4 * i + 3]) * inv);
+      for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * inv);
+      if (wide || !whole) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_global_v8(base + 8 * i, *reinterpret_cast<uint32_t(*)[8]>(&rr[8 * i]));
+      } else {
+        float4* d4 = reinterpret_cast<float4*>(base);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          d4[i] = make_float4(__uint_as_float(rr[4 * i]), __uint_as_float(rr[4 * i + 1]), __uint_as_float(rr[4 * i + 2]),
+                              __uint_as_float(rr[4 * i + 3]));
+      }
     }
   }
 }
