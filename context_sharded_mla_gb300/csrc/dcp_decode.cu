@@ -772,33 +772,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int seg = 0;
       bool ok = true;
       bool sent = false;  // this warp's rows of S_jglob have been shipped already
-      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
-        const int b = u / a.n_held, rs = u % a.n_held;
-        const int64_t S = a.seq_lens[b];
-        const int grow = g * Rg + row;
-        int64_t nvis = 0;  // keys of this shard visible to the row
-        if (row < Rg && grow < a.R_total && S >= a.q_len)
-          nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
-        // ---- query chunks 4r, 4r + 1 of the rows -> TMEM (thread t: chunk t / 16 of its row)
-        if (!wwait(&bars[kQEmpty], (seg & 1) ^ 1)) { ok = false; break; }
+      const int grow = g * Rg + row;
+      const bool has_row = row < Rg && grow < a.R_total;
+      // this warp's rows of the query chunks 4r, 4r + 1 (thread t: chunk t / 16 of
+      // its row) for request b
+      auto q_src = [&](int bq) {
+        return reinterpret_cast<const uint4*>(a.q + ((int64_t)bq * a.R_total + grow) * kDk + 256 * (int)rank +
+                                              kChunkDims * h);
+      };
+      // ... into TMEM for segment sq, once QK of segment sq - 1 no longer reads them
+      auto load_q = [&](int bq, int sq) -> bool {
+        if (!wwait(&bars[kQEmpty], (sq & 1) ^ 1)) return false;
         tc_fence_after();
-        {
-          const bool has_row = row < Rg && grow < a.R_total;
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.R_total + grow) * kDk +
-                                                            256 * (int)rank + kChunkDims * h);
-          uint32_t r[32];
+        const uint4* src = q_src(bq);
+        uint32_t r[32];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4 w4 = has_row ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-            r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
-          }
-          tmem_st16x2<32>(tmem + lane_addr + kQCol, r);
-          tmem_st_wait();
+        for (int k = 0; k < 8; ++k) {
+          uint4 w4 = has_row ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+          r[4 * k] = w4.x; r[4 * k + 1] = w4.y; r[4 * k + 2] = w4.z; r[4 * k + 3] = w4.w;
         }
+        tmem_st16x2<32>(tmem + lane_addr + kQCol, r);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kQFull]);
+        return true;
+      };
+      bool q_next = false;  // the next segment's query is already in TMEM
+      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+        const int b = u / a.n_held, rs = u % a.n_held;
+        if (!q_next && !load_q(b, seg)) { ok = false; break; }
+        q_next = false;
         ++seg;
+        // The next segment: its query rows into L2 now, into TMEM before this
+        // segment's epilogue, so that its first QK product overlaps the epilogue.
+        SegIter nx = it;
+        int32_t u2, t02, nt2, ks2;
+        bool wh2;
+        const bool has_next = nx.next(&u2, &t02, &nt2, &wh2, &ks2);
+        if (has_next && has_row) asm volatile("prefetch.global.L2 [%0];" ::"l"(q_src(u2 / a.n_held)));
+        const int64_t S = a.seq_lens[b];
+        int64_t nvis = 0;  // keys of this shard visible to the row
+        if (has_row && S >= a.q_len) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
         float m_ref = -INFINITY;  // running maximum of the row (log2 units)
         float l = 0.f;            // this thread's half of the row's running sum
         float l_row = 0.f;        // the row's running sum
@@ -903,6 +918,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars[kPFull0 + bsel]);
         }
         if (!ok) break;
+        if (has_next) {
+          if (!load_q(u2 / a.n_held, seg)) { ok = false; break; }
+          q_next = true;
+        }
         l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
         // ---------------- epilogue: O rows / l -> o (this CTA's 256 dims), lse
         const uint32_t jl = jglob - 1;
