@@ -302,29 +302,40 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
   tmem_st_wait();
 }
 
-// The same O rows times `inv` -> the output row (bf16 or fp32) or the fp32
-// piece row; thread t writes dims [d0, d0 + 128) of its row.  Each lane's
-// stores go to a different row, so they are made as wide as the alignment
-// allows (32 bytes: whole sectors, half the store instructions).  Kept out of
-// line: it runs once per segment and inlining it cost the tile loop.
-__device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, bool writes, bool whole,
-                                             int64_t out_row, int64_t piece_row, int d0, float inv) {
-  const bool wide = (reinterpret_cast<uintptr_t>(a.o_part) & 31) == 0;  // pieces are 256-byte aligned
+// v[idx] for idx in 0..3, without indexing registers at run time
+__device__ __forceinline__ uint32_t sel4(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, int idx) {
+  const uint32_t lo = (idx & 1) ? v1 : v0, hi = (idx & 1) ? v3 : v2;
+  return (idx & 2) ? hi : lo;
+}
+
+// The same O rows times `inv` -> the output rows (bf16 or fp32) or the fp32
+// piece rows; thread t holds dims [d0, d0 + 128) of row r0 + t % 16.  Rows
+// [0, rows_here) of the group are written.  Kept out of line: it runs once per
+// segment and inlining it cost the tile loop.
+//
+// fp32 rows: per 32 dims, the four lanes of each lane group (4 rows) trade
+// 32-byte blocks by shuffles (each lane offers a rotated block, then picks)
+// so that the group writes 128 contiguous bytes of one row per store: 8 lines
+// per warp store instead of 32.  bf16 rows: 32-byte stores, one row per lane.
+__device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int rows_here, bool whole,
+                                          int64_t out_base, int64_t piece_base, int r0, int d0, float inv) {
+  const int lane = threadIdx.x & 31;
+  const int row = r0 + (lane & 15);
+  if (whole && a.o_bf16) {
+    const bool wide = (reinterpret_cast<uintptr_t>(a.o_part) & 31) == 0;
 #pragma unroll 1
-  for (int k = 0; k < 4; ++k) {
-    uint32_t rr[32];
-    tmem_ld16x2<128>(o_addr + 32 * k, rr);
-    tmem_ld_wait();
-    if (!writes) continue;
-    const int d = d0 + 32 * k;
-    if (whole && a.o_bf16) {
+    for (int k = 0; k < 4; ++k) {
+      uint32_t rr[32];
+      tmem_ld16x2<128>(o_addr + 32 * k, rr);
+      tmem_ld_wait();
+      if (row >= rows_here) continue;
       uint32_t w[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
         w[e] = *reinterpret_cast<uint32_t*>(&hh);
       }
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_part) + out_row * kDv + d;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_part) + (out_base + row) * kDv + d0 + 32 * k;
       if (wide) {
         st_global_v8(dst, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
         st_global_v8(dst + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
@@ -333,19 +344,44 @@ __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, bool
 #pragma unroll
         for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
-    } else {
-      float* base = whole ? static_cast<float*>(a.o_part) + out_row * kDv + d : a.piece_o + piece_row * kDv + d;
+    }
+    return;
+  }
+  float* const out0 = whole ? static_cast<float*>(a.o_part) + out_base * kDv : a.piece_o + piece_base * kDv;
+  const bool wide = (reinterpret_cast<uintptr_t>(out0) & 31) == 0;  // pieces are 256-byte aligned
+  const int p = lane & 3, gl = lane & ~3;
+#pragma unroll 1
+  for (int k = 0; k < 4; ++k) {
+    uint32_t rr[32];
+    tmem_ld16x2<128>(o_addr + 32 * k, rr);
+    tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * inv);
-      if (wide || !whole) {
+    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * inv);
+    // step s: lane p offers its block (p + s) & 3 and takes block p of lane (p - s) & 3
+    uint32_t got[4][8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) st_global_v8(base + 8 * i, *reinterpret_cast<uint32_t(*)[8]>(&rr[8 * i]));
-      } else {
-        float4* d4 = reinterpret_cast<float4*>(base);
+    for (int s = 0; s < 4; ++s) {
+      const int ob = (p + s) & 3, src = gl | ((p - s) & 3);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          d4[i] = make_float4(__uint_as_float(rr[4 * i]), __uint_as_float(rr[4 * i + 1]), __uint_as_float(rr[4 * i + 2]),
-                              __uint_as_float(rr[4 * i + 3]));
+      for (int w = 0; w < 8; ++w)
+        got[s][w] = __shfl_sync(0xffffffffu, sel4(rr[w], rr[8 + w], rr[16 + w], rr[24 + w], ob), src);
+    }
+    // row of lane gl + q: its block p came at step (p - q) & 3
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int rq = r0 + ((gl | q) & 15), s = (p - q) & 3;
+      uint32_t v8[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v8[w] = sel4(got[0][w], got[1][w], got[2][w], got[3][w], s);
+      if (rq < rows_here) {
+        float* dst = out0 + (int64_t)rq * kDv + d0 + 32 * k + 8 * p;
+        if (wide) {
+          st_global_v8(dst, v8);
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(dst);
+          d4[0] = make_float4(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]), __uint_as_float(v8[3]));
+          d4[1] = make_float4(__uint_as_float(v8[4]), __uint_as_float(v8[5]), __uint_as_float(v8[6]), __uint_as_float(v8[7]));
+        }
       }
     }
   }
@@ -927,11 +963,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t jl = jglob - 1;
         if (!wwait(&bars[kPVDone0 + (jl & 1)], (jl >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const bool writes = row < min(Rg, a.R_total - g * Rg);
-        const int64_t out_row = ((int64_t)rs * a.B + b) * a.R_total + g * Rg + row;
-        const int64_t piece_row = (int64_t)(2 * v + kslot) * a.R_total + g * Rg + row;
+        const int rows_here = min(Rg, a.R_total - g * Rg);
+        const bool writes = row < rows_here;
+        const int64_t out_base = ((int64_t)rs * a.B + b) * a.R_total + g * Rg;
+        const int64_t piece_base = (int64_t)(2 * v + kslot) * a.R_total + g * Rg;
+        const int64_t out_row = out_base + row, piece_row = piece_base + row;
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        store_o_rows(a, tmem + lane_addr + kOCol, writes, whole, out_row, piece_row, 256 * (int)rank + 128 * h, inv);
+        store_o_rows(a, tmem + lane_addr + kOCol, rows_here, whole, out_base, piece_base, r0, 256 * (int)rank + 128 * h,
+                     inv);
         if (writes && h == 0 && rank == 0) {
           const float lse2 = l_row > 0.f ? m_ref + log2f(l_row) : -INFINITY;
           if (whole)
