@@ -9,27 +9,32 @@
 // "DCP x speculative decoding" (causal mask in global positions, from the shard
 // rank and the global lengths).
 //
-// Design: persistent 2-CTA clusters, one CTA per SM, 320 threads each:
+// Design: persistent 2-CTA clusters, one CTA per SM, 384 threads each:
+//   warps 0-7   softmax and score exchange: warp w serves 16 query rows
+//               (two threads per row, 32 keys each); it loads its rows of this
+//               CTA's query chunks into TMEM once per segment, ships its rows
+//               of each partial score tile to the peer, runs the online
+//               softmax and writes its rows of O at a segment end.
+//   warp 9      PV issuer (one thread).
 //   warp 10     TMA producer: this CTA's share of every KV tile (64 local rows)
-//               into a ring of tile slots; the query's shared-memory operands
-//               once per segment.  The warp fetches block-table entries 32
-//               tiles at a time.
-//   warp 11     tcgen05 issuer (one thread) and TMEM owner.
-//   warps 0-3   load this CTA's query chunks into TMEM once per segment, then
-//               softmax (one query row per thread) and epilogue.
-//   warps 4-7   send each partial score tile to the peer CTA.
+//               into a ring of tile slots, an L2 prefetch two tiles ahead, and
+//               the query's shared-memory operands once per segment.  The warp
+//               fetches block-table entries 32 tiles at a time.
+//   warp 11     QK issuer (one thread) and TMEM owner.
 // A cluster handles a group of at most 128 query rows.  The 576 key dims are
 // split between the two CTAs: CTA r loads value chunks 4r .. 4r + 3 (dims
-// [256 r, 256 r + 256), 128-byte swizzled boxes of 64 rows x 64 dims) and rope
-// dims [512 + 32 r, 512 + 32 r + 32) (64-byte swizzle).  Per tile j, in each CTA:
+// [256 r, 256 r + 256), one 3-D box of four 128-byte-swizzled 64 x 64 tiles)
+// and rope dims [512 + 32 r, 512 + 32 r + 32) (64-byte swizzle).  Per tile j,
+// in each CTA:
 //   S_j^r = Q[:, K_r] K_j[:, K_r]^T   M=128 rows, N=64 KV rows, K=288: query
-//                                     chunks 4r..4r+2 from TMEM, chunk 4r+3 and
-//                                     the rope half from shared memory -> TMEM fp32
-//   the sender warps stage S_j^r in shared memory and one bulk copy ships it to
-//   the peer (credited on the peer's mbarrier; two buffers per CTA swap the
-//   staging and receiving roles every tile) and each CTA forms S_j = S_j^0 + S_j^1
-//   (fp32 addition is commutative, so both CTAs hold the same bits and take
-//   the same softmax decisions);
+//                                     chunks 4r, 4r+1 from TMEM, chunks 4r+2,
+//                                     4r+3 and the rope half from shared
+//                                     memory -> TMEM fp32
+//   each softmax warp stages its rows of S_j^r in shared memory and one bulk
+//   copy ships them to the peer (credited on the peer's mbarrier; two buffers
+//   per CTA swap the staging and receiving roles every tile); each CTA forms
+//   S_j = S_j^0 + S_j^1 (fp32 addition is commutative, so both CTAs hold the
+//   same bits and take the same softmax decisions);
 //   P_j   = exp2(S_j*scale*log2e - m)  online softmax with lazy rescaling,
 //                                     bf16 pairs in their own TMEM columns
 //   O_r  += P_j V_j[:, dims of r]     M=128 rows (A = P from TMEM), N=256,
@@ -37,8 +42,8 @@
 // Each KV byte crosses HBM once and reaches one SM's shared memory once; the
 // tile's chunks stay in the ring from the QK product to the PV product (V = the
 // first 512 dims of the same rows).  TMEM per CTA: O (256 columns), two S
-// tiles (2 x 64), P (32) and three query chunks (96).  An S tile is free as
-// soon as its sender and softmax warps have read it, so QK products run up to
+// tiles (2 x 64), two P tiles (2 x 32) and two query chunks (64).  An S tile
+// is free as soon as every softmax warp has read it, so QK products run up to
 // two tiles ahead of the softmax while the exchange is in flight.
 //
 // Work split (stream-K): units are (request, shard); unit u has T_u tiles.  The
@@ -389,7 +394,7 @@ __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int 
 
 // ---------------------------------------------------------------------------- main kernel
 // A 2-CTA cluster per (work range, row group).  CTA `rank` loads key/value dims
-// [256 rank, 256 rank + 256) of every tile (CTA 0 also the 64 rope dims),
+// [256 rank, 256 rank + 256) and 32 rope dims of every tile,
 // computes its partial scores over them, swaps partial scores with its peer and
 // accumulates its own 256 value dims of O.  Both CTAs walk the same tile
 // sequence; the score exchange is double-buffered and S tiles are released as
