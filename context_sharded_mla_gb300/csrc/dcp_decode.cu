@@ -1004,12 +1004,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------- fixup
 // Writes empty units (o = 0, lse = -inf) and merges the pieces of units cut by
-// range boundaries (the same LSE rule as the shard merge, base 2).  One block
-// per unit: its piece list is built once in shared memory, then one warp per
-// query row merges the pieces with 16-byte loads and stores (lane l owns dims
-// [16 l, 16 l + 16)).
+// range boundaries (the same LSE rule as the shard merge, base 2).  Blocks
+// per unit: up to 12, each taking chunks of 8 query rows; thread 0 builds the
+// unit's piece list in shared memory, then one warp per row merges the pieces
+// with 16-byte loads and stores (lane l owns dims [16 l, 16 l + 16)).
 constexpr int kFixupThreads = 256;
 constexpr int kMaxPieces = 512;
+
+constexpr int kFixupRows = kFixupThreads / 32;  // query rows per block: one per warp
 
 __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   __shared__ int32_t piece_s[kMaxPieces];
@@ -1017,12 +1019,13 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   const int32_t U = a.B * a.n_held;
   const int32_t u = blockIdx.x;
   if (u >= U) return;
+  const int row0 = blockIdx.y * kFixupRows + (threadIdx.x >> 5);  // this warp's first query row
+  const int row_step = gridDim.y * kFixupRows;
   const int b = u / a.n_held, rs = u % a.n_held;
   const int64_t s = a.tile_start[u], e = a.tile_start[u + 1];
   const int64_t T = a.tile_start[U];
   const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kFixupThreads / 32;
+  const int lane = threadIdx.x & 31;
   auto store_row = [&](int64_t orow, const float (&v)[16]) {
     if (a.o_bf16) {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + orow * kDv + 16 * lane);
@@ -1046,7 +1049,7 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
     float z[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) z[i] = 0.f;
-    for (int row = warp; row < a.R_total; row += kWarps) {
+    for (int row = row0; row < a.R_total; row += row_step) {
       store_row(out_row0 + row, z);
       if (lane == 0) a.lse_part[out_row0 + row] = -INFINITY;
     }
@@ -1074,7 +1077,9 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   __syncthreads();
   const int np = npiece_s;
   if (np == 0) return;  // written whole by the main kernel
-  for (int row = warp; row < a.R_total; row += kWarps) {
+  for (int row = row0; row < a.R_total; row += row_step) {
+    // Pieces two at a time: both pieces' lse and o loads are issued before
+    // either is used (the row's loads are one latency, not one per piece).
     float m = -INFINITY;
     for (int k = 0; k < np; ++k) m = fmaxf(m, a.piece_lse[(int64_t)piece_s[k] * a.R_total + row]);
     float acc[16];
@@ -1082,20 +1087,29 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
-      for (int k = 0; k < np; ++k) {
-        const int64_t pr = (int64_t)piece_s[k] * a.R_total + row;
-        const float lv = a.piece_lse[pr];
-        if (lv == -INFINITY) continue;
-        const float w = exp2f(lv - m);
-        wsum += w;
-        const float4* src = reinterpret_cast<const float4*>(a.piece_o + pr * kDv + 16 * lane);
+      for (int k = 0; k < np; k += 2) {
+        const bool two = k + 1 < np;
+        const int64_t pr0 = (int64_t)piece_s[k] * a.R_total + row;
+        const int64_t pr1 = two ? (int64_t)piece_s[k + 1] * a.R_total + row : pr0;
+        const float4* src0 = reinterpret_cast<const float4*>(a.piece_o + pr0 * kDv + 16 * lane);
+        const float4* src1 = reinterpret_cast<const float4*>(a.piece_o + pr1 * kDv + 16 * lane);
+        float4 o0[4], o1[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float4 o4 = src[i];
-          acc[4 * i] = fmaf(w, o4.x, acc[4 * i]);
-          acc[4 * i + 1] = fmaf(w, o4.y, acc[4 * i + 1]);
-          acc[4 * i + 2] = fmaf(w, o4.z, acc[4 * i + 2]);
-          acc[4 * i + 3] = fmaf(w, o4.w, acc[4 * i + 3]);
+          o0[i] = src0[i];
+          o1[i] = src1[i];
+        }
+        const float l0 = a.piece_lse[pr0];
+        const float l1 = two ? a.piece_lse[pr1] : -INFINITY;
+        const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m);
+        const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m);
+        wsum += w0 + w1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[4 * i] = fmaf(w1, o1[i].x, fmaf(w0, o0[i].x, acc[4 * i]));
+          acc[4 * i + 1] = fmaf(w1, o1[i].y, fmaf(w0, o0[i].y, acc[4 * i + 1]));
+          acc[4 * i + 2] = fmaf(w1, o1[i].z, fmaf(w0, o0[i].z, acc[4 * i + 2]));
+          acc[4 * i + 3] = fmaf(w1, o1[i].w, fmaf(w0, o0[i].w, acc[4 * i + 3]));
         }
       }
     }
@@ -1305,7 +1319,10 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
   partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, tkv4, a);
-  fixup_kernel<<<U, kFixupThreads, 0, st>>>(a);
+  // one warp per row up to 96 rows; blocks loop over further row chunks (a large
+  // grid of blocks that mostly find their unit whole costs more than the loop)
+  const unsigned fix_y = (unsigned)std::min((a.R_total + kFixupRows - 1) / kFixupRows, 12);
+  fixup_kernel<<<dim3((unsigned)U, fix_y), kFixupThreads, 0, st>>>(a);
   return launch_status(3);
 }
 
