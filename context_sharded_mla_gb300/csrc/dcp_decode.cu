@@ -770,11 +770,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // [32 (t / 16), 32 (t / 16) + 32) of each tile (O columns [128 (t / 16), +128)).
     // Per tile j it reads its rows of this CTA's partial scores S_j^r, adds the
     // peer's (landed in buffer (j & 1) ^ 1) and runs the online softmax.  It also
-    // ships its rows of S_j^r to the peer: staged in buffer j & 1 and sent with
-    // one bulk copy, as soon as that buffer is free -- right after this warp has
-    // read the peer's tile j - 1 out of it (my copy of tile j - 1 out of the
-    // peer's buffer had landed by then), if S_j is ready, else at the start of
-    // tile j.  Both conditions are local, so no barrier guards the buffers.
+    // ships its rows of S_j^r to the peer, from the registers it has just read
+    // them into: staged in buffer j & 1 and sent with one bulk copy.  The buffer
+    // is free: this warp read the peer's tile j - 1 out of it in the previous
+    // tile, and my copy of tile j - 1 out of the peer's buffer had landed by
+    // then.  Both conditions are local, so no barrier guards the buffers.
+    // (Shipping S_{j+1} early, right after that read, was measured slower: the
+    // extra TMEM read and staging sit in the middle of the softmax.)
     // Waits are warp-wide and bounded, so a timeout drains every thread.
     const int r0 = 32 * (warp & 3) + kHalfRows * (warp >> 2);
     const int ch = warp;  // exchange channel
@@ -812,7 +814,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t jglob = 0;
       int seg = 0;
       bool ok = true;
-      bool sent = false;  // this warp's rows of S_jglob have been shipped already
       const int grow = g * Rg + row;
       const bool has_row = row < Rg && grow < a.R_total;
       // this warp's rows of the query chunks 4r, 4r + 1 (thread t: chunk t / 16 of
@@ -866,7 +867,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           tmem_ld16x2<32>(tmem + lane_addr + kSCol + kTile * bsel, s);
           tmem_ld_wait();
-          if (!sent) send(j, s);
+          send(j, s);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSFree0 + bsel]);
@@ -886,16 +887,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();  // every lane's reads of buffer rb are done
           if (lane == 0 && j + 2 < ntiles_cta)
             mbar_arrive_expect_tx(&bars[kXFull + 8 * rb + ch], kHalfRows * kXRowBytes);
-          // ---- buffer rb is free: ship S_{j+1} now if the product is done
-          sent = false;
-          if (j + 1 < ntiles_cta && __all_sync(0xffffffffu, mbar_test(&bars[kSFull0 + rb], ((j + 1) >> 1) & 1))) {
-            uint32_t s2[32];
-            tc_fence_after();
-            tmem_ld16x2<32>(tmem + lane_addr + kSCol + kTile * rb, s2);
-            tmem_ld_wait();
-            send(j + 1, s2);
-            sent = true;
-          }
           // ---- online softmax of tile j
           const int64_t lim = nvis - ((int64_t)(t0 + jj) * kTile + 32 * h);  // keys k < lim are visible
           if (lim < 32) {
