@@ -26,6 +26,14 @@ Sources
   page on each rank.  Reading used here: one block table per request, shared by
   all shards; shard r keeps its local row rho at bt[b][rho // P] * P + rho % P
   of its own pool.
+* "PCP / DCP：计算、KV 布局与块轮转", section "PD + DCP：从完整源页抽取本
+  rank 的 token": a request prefilled without DCP (full pages) is moved to a
+  DCP decode instance; rank r keeps the tokens whose request position it owns
+  (selected by request position, never by physical slot), reads each from its
+  source slot (source page * page size + offset) and writes them compactly into
+  its own pages; one transfer segment per token, merged into a longer segment
+  only where source and destination are both contiguous.  Section "Block RR
+  改善哪一段": with whole blocks per rank, whole contiguous pages move.
 """
 
 from __future__ import annotations
@@ -154,6 +162,55 @@ def kv_append(arena, kv_new_bits, pos, req, block_table, N: int, I: int, P: int,
         if shard_begin <= r < shard_end:
             arena[r - shard_begin, int(slot[t])] = kv_new_bits[t]
     return arena
+
+
+def pd_relayout(arena, src_pool_bits, src_block_table, src_P: int, pos, req, block_table,
+                N: int, I: int, P: int, shard_begin: int = 0, shard_end: int | None = None):
+    """Prefill-to-decode relayout of latent rows, in place (section "PD + DCP").
+
+    src_pool_bits: uint16 [src_rows, 576], the prefill side's paged pool (no
+    context sharding); request b's position p lives at source row
+    src_block_table[b][p // src_P] * src_P + p % src_P.  Each listed token
+    (pos[t] of request req[t]) goes to its owner's pool at the slot dcp
+    slot_map gives (owner by request position, compact local rows); tokens of
+    shards outside [shard_begin, shard_end) are skipped.  Returns the arena and
+    the (owner, source row, destination slot) of every token.
+    Raises LayoutError on a position, page index or page id out of range.
+    """
+    if shard_end is None:
+        shard_end = N
+    pos = np.asarray(pos, dtype=np.int64)
+    req = np.asarray(req, dtype=np.int64)
+    src = np.asarray(src_pool_bits)
+    # source side: one shard, pages of src_P rows (owner 0, local row = position)
+    _o, _r, src_row = slot_map(pos, req, src_block_table, 1, 1, src_P)
+    if np.any(src_row < 0) or np.any(src_row >= src.shape[0]):
+        raise LayoutError("source page id outside the source pool")
+    own, _row, dst = slot_map(pos, req, block_table, N, I, P)
+    arena = np.asarray(arena)
+    if np.any(dst < 0) or np.any(dst >= arena.shape[1]):
+        raise LayoutError("page id outside the pool")
+    for t in range(len(pos)):
+        r = int(own[t])
+        if shard_begin <= r < shard_end:
+            arena[r - shard_begin, int(dst[t])] = src[int(src_row[t])]
+    return arena, own, src_row, dst
+
+
+def relayout_segments(src_rows, dst_slots):
+    """Transfer segments (source row, destination slot, rows) of one rank's tokens.
+
+    Tokens in request order, one segment each; consecutive tokens are merged
+    only when both the source rows and the destination slots continue
+    contiguously (section "PD + DCP").
+    """
+    segs = []
+    for s_, d_ in zip(np.asarray(src_rows).tolist(), np.asarray(dst_slots).tolist()):
+        if segs and segs[-1][0] + segs[-1][2] == s_ and segs[-1][1] + segs[-1][2] == d_:
+            segs[-1][2] += 1
+        else:
+            segs.append([s_, d_, 1])
+    return [tuple(x) for x in segs]
 
 
 def accounting():

@@ -203,3 +203,81 @@ def test_layout_exhaustive_small():
         own = layout.owner(p, N, I)
         row = layout.local_row(p, N, I)
         assert all((int(own[i]), int(row[i])) == table[i] for i in range(60))
+
+
+def _src_pool(rows):
+    """A source pool whose row k holds the bit pattern k in every dim (uint16)."""
+    return np.repeat(np.arange(rows, dtype=np.uint16)[:, None], 576, axis=1)
+
+
+def test_pd_relayout_copies_the_worked_example():
+    """The owner-filtered copy moves exactly the page's 24 tokens, one segment each."""
+    g = golden("pd_relayout_rank1.json")
+    N, r, P = g["N"], g["rank"], g["P"]
+    pos = np.arange(g["request_tokens"])
+    src = _src_pool(16 * P)
+    arena = np.full((1, 16 * P, 576), 0xFFFF, dtype=np.uint16)
+    arena, own, src_row, dst = layout.pd_relayout(arena, src, np.array([g["source_pages"]]), P, pos,
+                                                  np.zeros_like(pos), np.array([[g["dest_page"]]]), N, 1, P,
+                                                  shard_begin=r, shard_end=r + 1)
+    mine = own == r
+    assert list(src_row[mine]) == g["source_slots"]
+    assert list(dst[mine]) == g["dest_slots"]
+    for s_, d_ in zip(g["source_slots"], g["dest_slots"]):
+        assert np.all(arena[0, d_] == s_)
+    written = np.nonzero(np.any(arena[0] != 0xFFFF, axis=1))[0]
+    assert list(written) == g["dest_slots"]          # nothing else in rank 1's pool changed
+    segs = layout.relayout_segments(src_row[mine], dst[mine])
+    assert len(segs) == g["tokens_received"] and all(n == 1 for _, _, n in segs)
+
+
+def test_pd_relayout_block_rr_moves_whole_pages():
+    """Block RR: request block k goes whole to rank k % N, as one contiguous segment."""
+    g = golden("pd_relayout_block_rr.json")
+    N, Bk, P = g["N"], g["block"], g["P"]
+    pos = np.arange(g["request_tokens"])
+    dst_page = 7
+    arena = np.zeros((N, 8 * P, 576), dtype=np.uint16)
+    arena, own, src_row, dst = layout.pd_relayout(arena, _src_pool(16 * P), np.array([g["source_pages"]]), P, pos,
+                                                  np.zeros_like(pos), np.array([[dst_page]]), N, Bk, P)
+    for k, r in enumerate(g["rank_of_block"]):
+        blk = own[k * Bk:(k + 1) * Bk]
+        assert np.all(blk == r)
+        segs = layout.relayout_segments(src_row[own == r], dst[own == r])
+        assert segs == [(g["source_pages"][k] * P, dst_page * P, Bk)]
+    assert [int(np.sum(own == r)) for r in range(N)] == g["rows_per_rank"]
+
+
+@pytest.mark.parametrize("N,I,P,srcP", [(8, 1, 64, 64), (4, 2, 16, 32), (3, 5, 20, 16), (16, 16, 64, 128)])
+def test_pd_relayout_matches_brute_force(N, I, P, srcP):
+    """Every token lands once, in its owner's pool at the dealt local row; chunk shares match count()."""
+    rng = np.random.default_rng(N * 100 + I)
+    B, L = 3, 300
+    a = np.array([0, 37, 1000])                       # chunk start of each request
+    pos = np.concatenate([np.arange(a[b], a[b] + L) for b in range(B)])
+    req = np.repeat(np.arange(B), L)
+    src_pages = (a + L + srcP - 1) // srcP
+    src_bt = np.full((B, int(src_pages.max())), -1, dtype=np.int64)
+    perm = rng.permutation(int(src_pages.sum()))
+    k = 0
+    for b in range(B):
+        src_bt[b, :src_pages[b]] = perm[k:k + src_pages[b]]
+        k += src_pages[b]
+    rows_per_b = [int(layout.count(0, a[b] + L, N, I)) + I for b in range(B)]
+    dpages = max((r + P - 1) // P for r in rows_per_b)
+    bt = rng.permutation(B * dpages).reshape(B, dpages)
+    src = rng.integers(0, 65535, size=(int(src_pages.sum()) * srcP, 576), dtype=np.uint16)
+    arena = np.zeros((N, B * dpages * P, 576), dtype=np.uint16)
+    arena, own, src_row, dst = layout.pd_relayout(arena, src, src_bt, srcP, pos, req, bt, N, I, P)
+    dealt = bruteforce.owner_row_table(int(a.max()) + L, N, I)
+    for t in range(len(pos)):
+        b, p = int(req[t]), int(pos[t])
+        r, rho = dealt[p]
+        assert own[t] == r
+        assert src_row[t] == src_bt[b, p // srcP] * srcP + p % srcP
+        assert dst[t] == bt[b, rho // P] * P + rho % P
+        assert np.array_equal(arena[r, dst[t]], src[src_row[t]])
+    for b in range(B):
+        for r in range(N):
+            got = int(np.sum((req == b) & (own == r)))
+            assert got == int(layout.count(r, a[b] + L, N, I) - layout.count(r, a[b], N, I))
