@@ -7,6 +7,7 @@ K3-shaped configuration (B=64, H=96, S=131072, N=8 token round-robin shards,
 page 64, base-2 LSE, one appended token per request per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3|dsv3|ragged|long|tiny]
+                  [--op decode|relayout]
                   [--impl ours|reference] [--batch B] [--no-cpu-baseline] [--no-e2e]
 
 `value` is KV-read GB/s (sum over requests of S_b * 1152 bytes per step,
@@ -290,6 +291,137 @@ def run_ours(args, cfg, rank, world, dist, device):
     return result
 
 
+RELAYOUT_METRIC = "prefill-to-decode relayout: moved KV GB/s (read + write), % of HBM roofline"
+RELAYOUT_SRC_PAGE = 64   # rows per page of the prefill-side pool
+
+
+def run_relayout_op(args, cfg, rank, world, dist, device):
+    """Timed dcp_kv_relayout: every token of the workload's requests, prefilled
+    without context sharding into a paged pool (pages of 64 rows, shuffled), is
+    moved into its owner's compact pool (all N shards on this GPU)."""
+    import context_sharded_mla_gb300 as dcp
+    lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
+    S = workloads.lengths(cfg)
+    g = torch.Generator(device=device).manual_seed(17)
+    Ps = RELAYOUT_SRC_PAGE
+    src_pages = [(int(x) + Ps - 1) // Ps for x in S]
+    total_src = sum(src_pages)
+    perm = torch.randperm(total_src, generator=g, device=device).to(torch.int32)
+    src_bt = torch.full((cfg.B, max(src_pages)), -1, dtype=torch.int32, device=device)
+    k = 0
+    for b in range(cfg.B):
+        src_bt[b, :src_pages[b]] = perm[k:k + src_pages[b]]
+        k += src_pages[b]
+    src_pool = torch.empty(total_src * Ps, 576, dtype=torch.bfloat16, device=device).normal_(generator=g)
+    bt, pool_pages = workloads.block_table(cfg, S)
+    bt = bt.to(device)
+    arena = torch.zeros(cfg.N, pool_pages * cfg.P, 576, dtype=torch.bfloat16, device=device)
+    pos = torch.cat([torch.arange(int(x), dtype=torch.int64, device=device) for x in S])
+    req = torch.cat([torch.full((int(x),), b, dtype=torch.int32, device=device) for b, x in enumerate(S)])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    T = pos.numel()
+    bytes_alg = T * (2 * 1152 + 12)           # read + write of each latent row, its position and request
+    stream = torch.cuda.current_stream()
+
+    def call(p_, r_):
+        dcp.dcp_kv_relayout(lay, 0, cfg.N, src_pool, Ps, src_bt, src_bt.shape[1], p_, r_, bt, bt.shape[1], arena,
+                            pool_pages, status)
+
+    for _ in range(args.warmup):
+        call(pos, req)
+    barrier(dist)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    launches0 = dcp.dcp_launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        call(pos, req)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    barrier(dist)
+    torch.cuda.profiler.stop()
+    launches = dcp.dcp_launch_count() - launches0
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed relayouts")
+    ms = max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    peaks = load_peaks()
+    achieved = bytes_alg / (kernel_ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        pos_h, req_h = pos.cpu().pin_memory(), req.cpu().pin_memory()
+        st_h = torch.empty(1, dtype=torch.int32).pin_memory()
+        pos_d, req_d = torch.empty_like(pos), torch.empty_like(req)
+
+        def e2e_step():
+            pos_d.copy_(pos_h, non_blocking=True)
+            req_d.copy_(req_h, non_blocking=True)
+            call(pos_d, req_d)
+            st_h.copy_(status, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        n = max(1, min(args.steps, 50))
+        a_ = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(n):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a_.elapsed_time(b_) / n
+        e2e = {"value": round(bytes_alg / (e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s", "ms_per_step": round(e_ms, 5),
+               "h2d_bytes_per_step": T * 12, "d2h_bytes_per_step": 4, "steps": n,
+               "path": "dcp_kv_relayout over the C ABI; token list copied from pinned host memory each step"}
+    return {
+        "metric": RELAYOUT_METRIC, "value": round(bytes_alg / (ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 latent rows, shuffled source and destination page tables)",
+        "config": {"workload": f"relayout of {workloads.DESCRIPTIONS.get(cfg.name, cfg.name)} requests, prefilled "
+                               f"without context sharding (source pages of {Ps} rows), into all {cfg.N} shards",
+                   "B": cfg.B, "tokens": T, "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P,
+                   "source_page_size": Ps, "l2": "source and destination far larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "kv_relayout_kernel (CUDA events on the launching stream)",
+                     "peak_source": f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured"
+                     else "fallback"},
+        "gpu_launches": launches, "e2e": e2e, "clocks": clk,
+    }
+
+
+def time_oracle_relayout(cfg, budget_s):
+    """The oracle's pd_relayout on a bounded sample: positions of one request of the same layout."""
+    import numpy as np
+    from oracle import layout as olayout
+    Ps = RELAYOUT_SRC_PAGE
+    rng = np.random.default_rng(5)
+    L = 65536
+    src_bt = rng.permutation(L // Ps)[None, :]
+    src = rng.integers(0, 65535, size=(L, 576), dtype=np.uint16)
+    rows = int(olayout.count(0, L, cfg.N, cfg.I)) + cfg.I
+    dpages = (rows + cfg.P - 1) // cfg.P
+    bt = rng.permutation(dpages)[None, :]
+    arena = np.zeros((cfg.N, dpages * cfg.P, 576), dtype=np.uint16)
+    pos = np.arange(L)
+    done, t0 = 0, time.time()
+    while done == 0 or time.time() - t0 < budget_s:  # whole passes over the request
+        olayout.pd_relayout(arena, src, src_bt, Ps, pos, np.zeros_like(pos), bt, cfg.N, cfg.I, cfg.P)
+        done += L
+    secs = time.time() - t0
+    return done * (2 * 1152 + 12), secs, (f"{done // L} pass(es) over one {L}-token request, same layout, "
+                                          "python/numpy, one thread")
+
+
 def run_e2e(args, cfg, st, dist, acct):
     dec = st["dec"]
     stream = torch.cuda.current_stream()
@@ -481,6 +613,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--op", default="decode", choices=["decode", "relayout"],
+                    help="decode: the decode step (default); relayout: the prefill-to-decode relayout")
     return ap.parse_args(argv)
 
 
@@ -502,6 +636,17 @@ def main(argv=None):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
+    if args.op == "relayout":
+        result = run_relayout_op(args, cfg, rank, world, dist, device)
+        if rank == 0 and not args.no_cpu_baseline:
+            nbytes, secs, desc = time_oracle_relayout(cfg, args.cpu_budget)
+            result["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": 1,
+                                      "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
     result = run_ours(args, cfg, rank, world, dist, device)
     if rank == 0 and not args.no_cpu_baseline:
         kv_bytes, secs, desc = time_oracle(cfg, args.cpu_budget, device=device)

@@ -9,7 +9,7 @@ works but the first call raises ``RuntimeError``.
 
 Functions (same names as the C ABI):
   dcp_count, dcp_slot_map, dcp_kv_append, dcp_mla_decode_partial,
-  dcp_mla_decode_workspace_size, dcp_lse_merge
+  dcp_mla_decode_workspace_size, dcp_lse_merge, dcp_kv_relayout
 """
 
 from __future__ import annotations
@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "DcpError", "Layout", "load_library", "library_path",
     "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
-    "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count",
+    "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count", "dcp_kv_relayout",
     "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes",
     "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
 ]
@@ -64,6 +64,8 @@ _SIGNATURES = {
     "dcp_count": (_I64, [_LP, _I32, _I64]),
     "dcp_slot_map": (_I32, [_LP, _P, _P, _I64, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "dcp_kv_append": (_I32, [_LP, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _P]),
+    "dcp_kv_relayout": (_I32, [_LP, _I32, _I32, _P, _I64, _I32, _P, _I64, _I64, _P, _P, _I64, _I32, _P, _I64, _I64,
+                               _P, _I64, _P, _P]),
     "dcp_mla_decode_partial": (_I32, [_LP, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _I64, _I64,
                                       _P, _F, _I32, _P, _I32, _P, _P, _SZ, _P, _P]),
     "dcp_mla_decode_workspace_size": (_SZ, [_LP, _I32, _I32, _I32, _I32, _I32]),
@@ -171,6 +173,28 @@ def dcp_kv_append(layout, shard_begin, shard_end, kv_new, owner, slot, arena, po
     _check("dcp_kv_append", load_library().dcp_kv_append(
         ctypes.byref(layout), shard_begin, shard_end, _ptr(kv_new), _ptr(owner), _ptr(slot), T,
         _ptr(arena), pool_pages, _ptr(status), _stream(stream)))
+
+
+def dcp_kv_relayout(layout, shard_begin, shard_end, src_pool, src_page_size, src_block_table, src_max_pages,
+                    pos, req, block_table, max_pages, arena, pool_pages, status, stream=None):
+    """Owner-filtered copy of tokens (pos, req) from a paged prefill pool src_pool [rows, 576] bf16."""
+    T = pos.shape[0]
+    _dev(src_pool, "src_pool", torch.bfloat16)
+    if src_pool.dim() != 2 or src_pool.shape[1] != 576:
+        raise ValueError("src_pool must be [rows, 576]")
+    _dev(src_block_table, "src_block_table", torch.int32)
+    _dev(pos, "pos", torch.int64, (T,))
+    _dev(req, "req", torch.int32, (T,))
+    _dev(block_table, "block_table", torch.int32)
+    _dev(arena, "arena", torch.bfloat16, (shard_end - shard_begin, pool_pages * layout.page_size, 576))
+    _dev(status, "status", torch.int32, (1,))
+    B, stride = block_table.shape
+    if src_block_table.shape[0] != B:
+        raise ValueError("src_block_table and block_table must have one row per request")
+    _check("dcp_kv_relayout", load_library().dcp_kv_relayout(
+        ctypes.byref(layout), shard_begin, shard_end, _ptr(src_pool), src_pool.shape[0], src_page_size,
+        _ptr(src_block_table), src_block_table.shape[1], src_max_pages, _ptr(pos), _ptr(req), T, B,
+        _ptr(block_table), stride, max_pages, _ptr(arena), pool_pages, _ptr(status), _stream(stream)))
 
 
 def dcp_mla_decode_workspace_size(layout, shard_begin, shard_end, B, q_len, H) -> int:

@@ -1,10 +1,14 @@
-// dcp_layout.cu — slot map and owner-filtered append (integer / copy kernels).
+// dcp_layout.cu — slot map, owner-filtered append and prefill-to-decode
+// relayout (integer / copy kernels).
 //
 // dcp_slot_map: one thread per new token computes (owner, local row, slot).
 // dcp_kv_append: one warp per new token copies its 1152-byte latent row with
 // 16-byte vector loads/stores into the owner's pool.  Both are tiny next to
 // the decode partial (B tokens per decode step; 8192 per chunk), so they are
 // written for latency: one launch each, no shared memory.
+// dcp_kv_relayout: one warp per listed token of a paged prefill pool: owner
+// filter, source and destination rows, a 1152-byte copy (HBM-bound for long
+// requests: 2 x 1152 bytes per moved token).
 #include "dcp_internal.cuh"
 
 #include <atomic>
@@ -95,7 +99,85 @@ __global__ void kv_append_kernel(const uint4* __restrict__ kv_new, const int32_t
   for (int i = lane; i < kVec; i += 32) dst[i] = __ldg(src + i);
 }
 
+// Prefill-to-decode relayout: one warp per listed token.  The owner filter
+// runs before any read, so tokens of other shards cost only their indices.
+// Positions below 2^31 (every realistic context) take 32-bit index math.
+__global__ void kv_relayout_kernel(Layout L, int32_t shard_begin, int32_t shard_end, const uint4* __restrict__ src,
+                                   int64_t src_rows, int32_t Ps, const int32_t* __restrict__ src_bt,
+                                   int64_t src_bt_stride, int64_t src_max_pages, const int64_t* __restrict__ pos,
+                                   const int32_t* __restrict__ req, int64_t T, int32_t B,
+                                   const int32_t* __restrict__ bt, int64_t bt_stride, int64_t max_pages,
+                                   uint4* __restrict__ arena, int64_t pool_rows, int32_t* status) {
+  constexpr int kVec = kDk * 2 / 16;  // 72 16-byte pieces per row
+  const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int64_t p = __ldg(pos + t);
+  const int32_t b = __ldg(req + t);
+  if (p < 0 || b < 0 || b >= B) {
+    if (lane == 0) flag(status, p < 0 ? DCP_STATUS_BAD_POSITION : DCP_STATUS_BAD_REQUEST);
+    return;
+  }
+  int64_t own, row, src_pidx, src_off;
+  if (p < INT32_MAX) {
+    const int32_t p32 = (int32_t)p, blk = p32 / L.I;
+    own = blk % L.N;
+    row = (int64_t)(blk / L.N) * L.I + p32 % L.I;
+    src_pidx = p32 / Ps;
+    src_off = p32 % Ps;
+  } else {
+    own = owner_of(p, L);
+    row = local_row_of(p, L);
+    src_pidx = p / Ps;
+    src_off = p % Ps;
+  }
+  if (own < shard_begin || own >= shard_end) return;  // another device's shard
+  const int64_t pidx = row / L.P;
+  if (src_pidx >= src_max_pages || pidx >= max_pages) {
+    if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_INDEX);
+    return;
+  }
+  const int64_t sp = __ldg(src_bt + (int64_t)b * src_bt_stride + src_pidx);
+  const int64_t dp = __ldg(bt + (int64_t)b * bt_stride + pidx);
+  const int64_t srow = sp * Ps + src_off, drow = dp * L.P + row % L.P;
+  if (sp < 0 || srow >= src_rows || dp < 0 || drow >= pool_rows) {
+    if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_ID);
+    return;
+  }
+  const uint4* s = src + srow * kVec;
+  uint4* d = arena + ((int64_t)(own - shard_begin) * pool_rows + drow) * kVec;
+  uint4 v0 = __ldg(s + lane), v1 = __ldg(s + 32 + lane), v2;
+  if (lane < kVec - 64) v2 = __ldg(s + 64 + lane);
+  d[lane] = v0;
+  d[32 + lane] = v1;
+  if (lane < kVec - 64) d[64 + lane] = v2;
+}
+
 }  // namespace
+
+extern "C" int32_t dcp_kv_relayout(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                                   const void* src_pool, int64_t src_pool_rows, int32_t src_page_size,
+                                   const int32_t* src_block_table, int64_t src_bt_stride, int64_t src_max_pages,
+                                   const int64_t* pos, const int32_t* req, int64_t T, int32_t B,
+                                   const int32_t* block_table, int64_t bt_stride, int64_t max_pages, void* arena,
+                                   int64_t pool_pages, int32_t* status, void* stream) {
+  if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end ||
+      T < 0 || B < 1 || src_page_size < 1 || src_pool_rows < 1 || pool_pages < 1 || src_max_pages < 1 ||
+      src_bt_stride < src_max_pages || max_pages < 1 || bt_stride < max_pages)
+    return DCP_ERR_INVALID;
+  if (T == 0) return DCP_OK;
+  if (!src_pool || !src_block_table || !pos || !req || !block_table || !arena || !status) return DCP_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(src_pool) | reinterpret_cast<uintptr_t>(arena)) & 15)
+    return DCP_ERR_INVALID;  // rows are moved as 16-byte vectors
+  const int threads = 256;  // 8 tokens per block
+  const int64_t blocks = (T * 32 + threads - 1) / threads;
+  if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
+  kv_relayout_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(
+      to_layout(layout), shard_begin, shard_end, static_cast<const uint4*>(src_pool), src_pool_rows, src_page_size,
+      src_block_table, src_bt_stride, src_max_pages, pos, req, T, B, block_table, bt_stride, max_pages,
+      static_cast<uint4*>(arena), pool_pages * layout->page_size, status);
+  return launch_status();
+}
 
 extern "C" int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32_t* req,
                                 int64_t T, const int32_t* block_table, int32_t B, int64_t bt_stride,

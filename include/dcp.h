@@ -8,6 +8,8 @@
  *   2. dcp_kv_append           owner-filtered write of the 576-d latent rows
  *   3. dcp_mla_decode_partial  per-shard partial attention (o_r, lse_r)
  *   4. dcp_lse_merge           exact log-sum-exp merge of the N partials
+ * and, for moving a request prefilled without context sharding into the shards,
+ *   5. dcp_kv_relayout         owner-filtered copy from a paged prefill pool
  *
  * On one GPU the N context shards are N compact paged pools in one HBM
  * allocation (the "arena"), so the cross-rank steps (query all-gather,
@@ -151,6 +153,44 @@ int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32
 int32_t dcp_kv_append(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
                       const void* kv_new, const int32_t* owner, const int64_t* slot, int64_t T,
                       void* arena, int64_t pool_pages, int32_t* status, void* stream);
+
+/*
+ * dcp_kv_relayout — prefill-to-decode relayout of latent rows into the shards.
+ *
+ * Source: "PCP / DCP：计算、KV 布局与块轮转", section "PD + DCP：从完整源页
+ * 抽取本 rank 的 token" (a request prefilled without context sharding, in full
+ * pages, moves to a DCP decode instance: each rank keeps the tokens whose
+ * request position it owns -- chosen by position, not by physical slot --
+ * reads them from their source slots and writes them compactly into its own
+ * pages) and section "Block RR 改善哪一段" (with block round-robin whole
+ * contiguous pages move).
+ *
+ *   src_pool         bf16[src_pool_rows, 576]  the prefill side's paged pool
+ *   src_block_table  int32[B, src_bt_stride]; entry [b][k] is the source page
+ *                    holding request positions [k*src_page_size, (k+1)*src_page_size)
+ *                    of b; only columns k < src_max_pages are read
+ *   pos, req         int64[T], int32[T]: the request position and request of
+ *                    each token to move (e.g. positions [a, a+L) of a chunk)
+ *   block_table, arena, pool_pages: the decode side, as in dcp_slot_map and
+ *                    dcp_kv_append (arena holds shards [shard_begin, shard_end))
+ * Token t with owner(pos[t]) in [shard_begin, shard_end) is copied bit for bit
+ * from src_pool[src_block_table[req][pos / src_page_size] * src_page_size +
+ * pos % src_page_size] to arena[owner - shard_begin][slot], slot as in
+ * dcp_slot_map; tokens of other shards are neither read nor written.  A
+ * negative position, a request outside [0, B), a page index past max_pages /
+ * src_max_pages, or a page id whose rows fall outside the pool (source or
+ * destination) sets the DCP_STATUS_* bit and skips that token.  src_pool and
+ * arena must not overlap.  T == 0 is a no-op.  Errors: DCP_ERR_INVALID for a
+ * bad layout or shard range, T < 0, B < 1, src_page_size < 1, max_pages or
+ * src_max_pages outside [1, stride], pool sizes < 1, a null pointer with T > 0,
+ * or src_pool / arena not 16-byte aligned.
+ */
+int32_t dcp_kv_relayout(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                        const void* src_pool, int64_t src_pool_rows, int32_t src_page_size,
+                        const int32_t* src_block_table, int64_t src_bt_stride, int64_t src_max_pages,
+                        const int64_t* pos, const int32_t* req, int64_t T, int32_t B,
+                        const int32_t* block_table, int64_t bt_stride, int64_t max_pages, void* arena,
+                        int64_t pool_pages, int32_t* status, void* stream);
 
 /*
  * dcp_mla_decode_partial — locally normalised partial attention of each shard.

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
-              "dcp_mla_decode_workspace_size", "dcp_lse_merge"]:
+              "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_kv_relayout"]:
         assert n in names
 
 
@@ -90,6 +90,27 @@ def test_host_validation_rejects_bad_arguments(lib):
     need = lib.dcp_mla_decode_workspace_size(ctypes.byref(good), 0, 4, 1, 1, 16)
     if need > 0:
         assert call(wsb=need - 1, ws=P(256)) == -4
+    # prefill-to-decode relayout
+    rl = lambda **kw: dict(dict(sb=0, se=4, src=P(256), srows=64, sps=16, sbt=P(256), sst=1, smp=1, pos=P(256),
+                                req=P(256), T=1, B=1, bt=P(256), st=1, mp=1, ar=P(256), pp=1, status=P(256)), **kw)
+
+    def relayout(**kw):
+        a = rl(**kw)
+        return lib.dcp_kv_relayout(ctypes.byref(good), a["sb"], a["se"], a["src"], a["srows"], a["sps"], a["sbt"],
+                                   a["sst"], a["smp"], a["pos"], a["req"], a["T"], a["B"], a["bt"], a["st"],
+                                   a["mp"], a["ar"], a["pp"], a["status"], None)
+    assert relayout(T=0) == 0                       # no-op, nothing launched
+    assert relayout(se=5) == -1
+    assert relayout(sb=2, se=2) == -1
+    assert relayout(sps=0) == -1
+    assert relayout(smp=2, sst=1) == -1
+    assert relayout(mp=0) == -1
+    assert relayout(B=0) == -1
+    assert relayout(src=P(264)) == -1               # not 16-byte aligned
+    assert relayout(src=None) == -1
+    assert relayout(status=None) == -1
+    assert lib.dcp_kv_relayout(ctypes.byref(bad), 0, 4, P(256), 64, 16, P(256), 1, 1, P(256), P(256), 1, 1, P(256),
+                               1, 1, P(256), 1, P(256), None) == -1
     # merge
     assert lib.dcp_lse_merge(0, 10, P(256), 0, P(256), 0, P(256), 0, P(256), None) == -1
     assert lib.dcp_lse_merge(2, 10, P(256), 3, P(256), 0, P(256), 0, P(256), None) == -1
