@@ -104,7 +104,7 @@ def workload_accounting(cfg, S_b):
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -119,9 +119,13 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self):
+        """Host time at the edge of the timed region (the sampler keeps only samples between marks)."""
+        self.marks = getattr(self, "marks", []) + [time.time()]
 
     def stop(self):
         if self.proc is None:
@@ -132,25 +136,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        import datetime
+        lo, hi = (self.marks[0], self.marks[-1]) if len(getattr(self, "marks", [])) >= 2 else (None, None)
+        sm, mx, reasons, all_sm = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, cmax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                all_sm.append(clk)
+                # samples inside the timed region (100 ms sampling: allow one period of slack)
+                if lo is not None and not (lo - 0.1 <= ts <= hi + 0.1):
+                    continue
+                sm.append(clk)
+                mx.append(cmax)
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "window": "timed region only"}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -225,6 +237,7 @@ def run_ours(args, cfg, rank, world, dist, device):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.profiler.start()           # bounds an `ncu --profile-from-start off` launch list
+    clocks.mark()
     t0.record(stream)
     for i in range(args.steps):
         ev_step[i][0].record(stream)
@@ -232,6 +245,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         ev_step[i][1].record(stream)
     t1.record(stream)
     barrier(dist)
+    clocks.mark()
     torch.cuda.profiler.stop()
     launches = dcp.dcp_launch_count() - launches0
     clk = clocks.stop()
@@ -339,6 +353,7 @@ def run_relayout_op(args, cfg, rank, world, dist, device):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.profiler.start()
+    clocks.mark()
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -346,6 +361,7 @@ def run_relayout_op(args, cfg, rank, world, dist, device):
         ev[i][1].record(stream)
     t1.record(stream)
     barrier(dist)
+    clocks.mark()
     torch.cuda.profiler.stop()
     launches = dcp.dcp_launch_count() - launches0
     clk = clocks.stop()
