@@ -13,10 +13,11 @@ The oracle is written from these pages (quoted by title and section):
   slot, owner(p) = p mod N, row(p) = floor(p / N), chunk share
   count(a+L) - count(a); idea 2: each shard hands over (O_r, L_r)), section
   "Theory" (derivation of the merge identity, the merge operator and its
-  numerically stable form, the base-e / base-2 pairing rule).
+  numerically stable form, the base-e / base-2 pairing rule);
+  section "decode 路径：以 Kimi K3 的 MLA 为例" (w_kc / w_vc shapes).
 * "MLA 的 Decode Context Parallelism" (ggaaooppeenngg.github.io): section 2
-  (absorbed form: 576-d single-KV-head MQA, V = the 512-d c_K part) and
-  section 3 (the two-pass LSE merge).
+  (absorbed form: 576-d single-KV-head MQA, V = the 512-d c_K part, and the
+  two absorption identities) and section 3 (the two-pass LSE merge).
 * "PCP / DCP：计算、KV 布局与块轮转" (obnotes-4iw.pages.dev): section 5 (token
   round-robin), section 6 (block round-robin owner / local_index / local_len),
   section "KV cache 管理" (slot = page_id * page_size + offset).
@@ -33,9 +34,10 @@ Modules
 ``layout``      slot math, chunk share, vLLM virtual-block map, owner-filtered append.
 ``attention``   per-shard partial (o_r, lse_r), LSE merge, unsharded attention.
 ``bruteforce``  pure-Python loop versions for tiny inputs (pins for the above).
+``absorb``      the query-side and output-side absorption products (identities 1, 2).
 
 Every function here is pinned by a ``-m "not gpu"`` test against the pages'
 worked examples, closed forms, invariants or brute force.  None is unpinned.
 """
 
-from . import layout, attention, bruteforce  # noqa: F401
+from . import layout, attention, bruteforce, absorb  # noqa: F401
