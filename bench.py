@@ -7,7 +7,7 @@ K3-shaped configuration (B=64, H=96, S=131072, N=8 token round-robin shards,
 page 64, base-2 LSE, one appended token per request per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3|dsv3|ragged|long|tiny]
-                  [--op decode|relayout]
+                  [--op decode|relayout|absorb]
                   [--impl ours|reference] [--batch B] [--no-cpu-baseline] [--no-e2e]
 
 `value` is KV-read GB/s (sum over requests of S_b * 1152 bytes per step,
@@ -438,6 +438,148 @@ def time_oracle_relayout(cfg, budget_s):
                                           "python/numpy, one thread")
 
 
+ABSORB_METRIC = "absorption products (q_nope @ w_kc, o @ w_vc): moved GB/s, % of HBM roofline"
+L2_FLUSH_BYTES = 256 << 20      # written between timed steps: twice the 129 MB L2
+
+
+def absorb_bytes(T, H, o_bytes_per_el=2, v_bytes_per_el=2):
+    """Algorithmic bytes of one pass of each product: (query side, output side)."""
+    q_side = T * H * (128 + 64) * 2 + H * 128 * 512 * 2 + T * H * 576 * 2
+    o_side = T * H * 512 * o_bytes_per_el + H * 512 * 128 * 2 + T * H * 128 * v_bytes_per_el
+    return q_side, o_side
+
+
+def run_absorb_op(args, cfg, rank, world, dist, device):
+    """Timed dcp_absorb_q + dcp_absorb_o at the workload's decode shapes (T = B x q_len
+    query tokens, H heads; synthetic bf16 weights; o in the merge's output dtype)."""
+    import context_sharded_mla_gb300 as dcp
+    T, H = cfg.B * cfg.q_len, cfg.H
+    qp = workloads.gen_q_proj(cfg, device)
+    w_kc, w_vc = (w.to(device) for w in workloads.gen_absorb_weights(cfg, device))
+    o_dtype = torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(23)
+    o = torch.randn(cfg.B, cfg.q_len, H, 512, generator=g, device=device).to(o_dtype)
+    q = torch.empty(cfg.B, cfg.q_len, H, 576, dtype=torch.bfloat16, device=device)
+    v = torch.empty(cfg.B, cfg.q_len, H, 128, dtype=torch.bfloat16, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    q_bytes, o_bytes = absorb_bytes(T, H, o.element_size(), 2)
+    stream = torch.cuda.current_stream()
+
+    def call(qp_, o_):
+        dcp.dcp_absorb_q(qp_[..., :128], qp_[..., 128:], w_kc, q, status)
+        dcp.dcp_absorb_o(o_, w_vc, v, status)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call(qp, o)
+    barrier(dist)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    launches0 = dcp.dcp_launch_count()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.profiler.start()
+    clocks.mark()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 cold for every step (outside the kernel events)
+        ev[i][0].record(stream)
+        dcp.dcp_absorb_q(qp[..., :128], qp[..., 128:], w_kc, q, status)
+        ev[i][1].record(stream)
+        dcp.dcp_absorb_o(o, w_vc, v, status)
+        ev[i][2].record(stream)
+    barrier(dist)
+    clocks.mark()
+    torch.cuda.profiler.stop()
+    launches = dcp.dcp_launch_count() - launches0
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed absorption products")
+    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    o_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms = max_over_ranks(dist, q_ms + o_ms)
+    peaks = load_peaks()
+    dom = ("absorb_kernel (query side)", q_bytes, q_ms) if q_ms >= o_ms else ("absorb_kernel (output side)",
+                                                                              o_bytes, o_ms)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        qp_h = qp.cpu().pin_memory()
+        o_h = o.cpu().pin_memory()
+        q_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        v_h = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+        qp_d, o_d = torch.empty_like(qp), torch.empty_like(o)
+
+        def e2e_step():
+            qp_d.copy_(qp_h, non_blocking=True)
+            o_d.copy_(o_h, non_blocking=True)
+            call(qp_d, o_d)
+            q_h.copy_(q, non_blocking=True)
+            v_h.copy_(v, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        n = max(1, min(args.steps, 200))
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(n):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a_.elapsed_time(b_) / n
+        e2e = {"value": round((q_bytes + o_bytes) / (e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 5),
+               "h2d_bytes_per_step": qp.numel() * 2 + o.numel() * o.element_size(),
+               "d2h_bytes_per_step": q.numel() * 2 + v.numel() * 2, "steps": n,
+               "path": "dcp_absorb_q + dcp_absorb_o over the C ABI; q_proj and o copied from pinned host memory, "
+                       "q and v copied back, every step (weights resident)"}
+    return {
+        "metric": ABSORB_METRIC, "value": round((q_bytes + o_bytes) / (ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) query projection and o; weights N(0, 1/fan_in), bf16)",
+        "config": {"workload": f"absorption products at the decode shapes of "
+                               f"{workloads.DESCRIPTIONS.get(cfg.name, cfg.name)}: T={T} query tokens, H={H}, "
+                               f"w_kc [H,128,512], w_vc [H,512,128], o {str(o_dtype).split('.')[-1]}, v bf16",
+                   "T": T, "H": H, "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write, "
+                                          "outside the timed kernels)"},
+        "kernels_us": {"absorb_q": round(q_ms * 1e3, 3), "absorb_o": round(o_ms * 1e3, 3)},
+        "bytes_alg": {"absorb_q": q_bytes, "absorb_o": o_bytes},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": f"{dom[0]} (CUDA events on the launching stream)",
+                     "peak_source": f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured"
+                     else "fallback"},
+        "gpu_launches": launches, "e2e": e2e, "clocks": clk,
+    }
+
+
+def time_oracle_absorb(cfg, budget_s):
+    """The oracle's absorb_q + absorb_o on a bounded sample: all T tokens, a slice of the heads per pass."""
+    import numpy as np
+    from oracle import absorb as oabsorb
+    T, H = cfg.B * cfg.q_len, cfg.H
+    qp = workloads.gen_q_proj(cfg).reshape(T, H, 192).to(torch.float64).numpy()
+    w_kc, w_vc = (w.to(torch.float64).numpy() for w in workloads.gen_absorb_weights(cfg))
+    o = np.random.default_rng(23).standard_normal((T, H, 512))
+    hs = max(1, min(H, 8))
+    q_bytes, o_bytes = absorb_bytes(T, H, 2, 2)
+    done, t0 = 0, time.time()
+    while done == 0 or time.time() - t0 < budget_s:
+        h0 = (done * hs) % H
+        sl = slice(h0, min(H, h0 + hs))
+        oabsorb.absorbed_query(qp[:, sl, :128], qp[:, sl, 128:], w_kc[sl])
+        oabsorb.absorb_o(o[:, sl], w_vc[sl])
+        done += 1
+    secs = time.time() - t0
+    heads = done * hs
+    return (q_bytes + o_bytes) * heads / H, secs, (f"{done} passes of {hs} of {H} heads x {T} tokens (both "
+                                                    f"products, fp64 numpy einsum); throughput counts that share "
+                                                    f"of the algorithmic bytes")
+
+
 def run_e2e(args, cfg, st, dist, acct):
     dec = st["dec"]
     stream = torch.cuda.current_stream()
@@ -616,6 +758,32 @@ def run_reference(args, cfg, rank, world):
     }
 
 
+def run_reference_op(args, cfg, rank, world):
+    """--impl reference for --op relayout / absorb: the oracle of that op, timed per step on a bounded sample."""
+    if rank != 0:
+        return None
+    metric, time_op = ((RELAYOUT_METRIC, time_oracle_relayout) if args.op == "relayout"
+                       else (ABSORB_METRIC, time_oracle_absorb))
+    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_op(cfg, budget)
+    nbytes, secs = 0.0, 0.0
+    for _ in range(args.steps):
+        b_, s_, desc = time_op(cfg, budget)
+        nbytes, secs = nbytes + b_, secs + s_
+    value = nbytes / secs / 1e9
+    return {
+        "metric": metric, "impl": "reference", "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": workloads.DESCRIPTIONS.get(cfg.name, cfg.name),
+                                                  "op": args.op},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # ----------------------------------------------------------------------------- main
 
 def parse(argv=None):
@@ -629,8 +797,9 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--op", default="decode", choices=["decode", "relayout"],
-                    help="decode: the decode step (default); relayout: the prefill-to-decode relayout")
+    ap.add_argument("--op", default="decode", choices=["decode", "relayout", "absorb"],
+                    help="decode: the decode step (default); relayout: the prefill-to-decode relayout; "
+                         "absorb: the two absorption products")
     return ap.parse_args(argv)
 
 
@@ -643,7 +812,8 @@ def main(argv=None):
     if args.batch:
         cfg = workloads.config(args.workload, B=args.batch)
     if args.impl == "reference":
-        out = run_reference(args, cfg, rank, world)
+        out = (run_reference(args, cfg, rank, world) if args.op == "decode"
+               else run_reference_op(args, cfg, rank, world))
         if out is not None:
             print(json.dumps(out), flush=True)
         return 0
@@ -652,10 +822,12 @@ def main(argv=None):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
-    if args.op == "relayout":
-        result = run_relayout_op(args, cfg, rank, world, dist, device)
+    if args.op in ("relayout", "absorb"):
+        run_op, time_op = ((run_relayout_op, time_oracle_relayout) if args.op == "relayout"
+                           else (run_absorb_op, time_oracle_absorb))
+        result = run_op(args, cfg, rank, world, dist, device)
         if rank == 0 and not args.no_cpu_baseline:
-            nbytes, secs, desc = time_oracle_relayout(cfg, args.cpu_budget)
+            nbytes, secs, desc = time_op(cfg, args.cpu_budget)
             result["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": 1,
                                       "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
         if rank == 0:

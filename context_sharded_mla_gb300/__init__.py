@@ -9,7 +9,8 @@ works but the first call raises ``RuntimeError``.
 
 Functions (same names as the C ABI):
   dcp_count, dcp_slot_map, dcp_kv_append, dcp_mla_decode_partial,
-  dcp_mla_decode_workspace_size, dcp_lse_merge, dcp_kv_relayout
+  dcp_mla_decode_workspace_size, dcp_lse_merge, dcp_kv_relayout, dcp_absorb_q,
+  dcp_absorb_o
 """
 
 from __future__ import annotations
@@ -25,7 +26,7 @@ __all__ = [
     "DcpError", "Layout", "load_library", "library_path",
     "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
     "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count", "dcp_kv_relayout",
-    "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes",
+    "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes", "dcp_absorb_q", "dcp_absorb_o",
     "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
 ]
 
@@ -73,6 +74,8 @@ _SIGNATURES = {
     "dcp_mla_decode_partial_static": (_I32, [_LP, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _I64, _I64,
                                              _P, _F, _I32, _P, _I32, _P, _P, _P]),
     "dcp_mla_decode_static_scratch_bytes": (_SZ, []),
+    "dcp_absorb_q": (_I32, [_I64, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P]),
+    "dcp_absorb_o": (_I32, [_I64, _I32, _P, _I32, _P, _P, _I32, _P, _P]),
 }
 
 
@@ -277,3 +280,56 @@ def dcp_mla_decode_partial_static(layout, shard_begin, shard_end, q, arena, pool
         ctypes.byref(layout), shard_begin, shard_end, _ptr(q), B, q_len, H, _ptr(arena), pool_pages,
         _ptr(block_table), block_table.shape[1], max_pages, _ptr(seq_lens), float(scale), lse_base,
         _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), _ptr(status), _stream(stream)))
+
+
+def _rows(t, name, width):
+    """Row stride (elements) of a bf16 CUDA view [..., width] whose rows are equally strided."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be torch.bfloat16, got {t.dtype}")
+    if t.shape[-1] != width or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be [..., {width}] with a contiguous last dim")
+    row = t.stride(-2) if t.dim() >= 2 else width
+    for i in range(t.dim() - 2):
+        if t.shape[i + 1] > 1 and t.stride(i) != t.stride(i + 1) * t.shape[i + 1]:
+            raise ValueError(f"{name}'s rows must be equally strided")
+    return row
+
+
+def dcp_absorb_q(q_nope, q_pe, w_kc, q, status=None, stream=None):
+    """q [..., H, 576] = [q_nope @ w_kc[h] || q_pe] per head.
+
+    q_nope [..., H, 128] and q_pe [..., H, 64] are bf16 views with a contiguous
+    last dim and equally strided rows (slices of a [..., H, 192] q_b_proj output
+    qualify); w_kc [H, 128, 512] bf16; q contiguous bf16."""
+    H = w_kc.shape[0]
+    _dev(w_kc, "w_kc", torch.bfloat16, (H, 128, 512))
+    _dev(q, "q", torch.bfloat16)
+    if q.dim() < 2 or q.shape[-1] != 576 or q.shape[-2] != H:
+        raise ValueError(f"q must be [..., {H}, 576]")
+    T = q.numel() // (H * 576)
+    sn, sp = _rows(q_nope, "q_nope", 128), _rows(q_pe, "q_pe", 64)
+    if q_nope.shape[:-1] != q.shape[:-1] or q_pe.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q_nope, q_pe and q must have the same leading dims")
+    if status is not None:
+        _dev(status, "status", torch.int32, (1,))
+    _check("dcp_absorb_q", load_library().dcp_absorb_q(
+        T, H, _ptr(q_nope), sn, _ptr(q_pe), sp, _ptr(w_kc), _ptr(q), _ptr(status), _stream(stream)))
+
+
+def dcp_absorb_o(o, w_vc, v, status=None, stream=None):
+    """v [..., H, 128] = o [..., H, 512] @ w_vc[h] per head (o, v f32 or bf16; w_vc [H, 512, 128] bf16)."""
+    H = w_vc.shape[0]
+    _dev(w_vc, "w_vc", torch.bfloat16, (H, 512, 128))
+    _dev(o, "o", o.dtype)
+    _dev(v, "v", v.dtype)
+    if o.dim() < 2 or o.shape[-1] != 512 or o.shape[-2] != H:
+        raise ValueError(f"o must be [..., {H}, 512]")
+    if v.shape[:-1] != o.shape[:-1] or v.shape[-1] != 128:
+        raise ValueError(f"v must be [..., {H}, 128] with o's leading dims")
+    if status is not None:
+        _dev(status, "status", torch.int32, (1,))
+    T = o.numel() // (H * 512)
+    _check("dcp_absorb_o", load_library().dcp_absorb_o(
+        T, H, _ptr(o), _dtype_code(o), _ptr(w_vc), _ptr(v), _dtype_code(v), _ptr(status), _stream(stream)))

@@ -1186,27 +1186,13 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   return nts >= 3;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // bf16 [rows, 576] row-major, boxes of [box_rows, 64] with 128-byte swizzle, or
 // (half = true) boxes of [box_rows, 32] with 64-byte swizzle
 // bf16 [rows, 576] seen as [9 chunks][rows][64 dims] (dims innermost, then rows,
 // then chunks 128 bytes apart): boxes of [4 chunks][box_rows][64] land as four
 // consecutive 128-byte-swizzled [box_rows][64] tiles.
 bool make_tmap_chunks(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  auto enc = encode_fn();
+  auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kChunkDims, (cuuint64_t)rows, (cuuint64_t)(kDk / kChunkDims)};
   cuuint64_t strides[2] = {(cuuint64_t)kDk * 2, (cuuint64_t)kChunkDims * 2};
@@ -1218,7 +1204,7 @@ bool make_tmap_chunks(CUtensorMap* m, const void* base, uint64_t rows, uint32_t 
 }
 
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool half = false) {
-  auto enc = encode_fn();
+  auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};

@@ -10,6 +10,9 @@
  *   4. dcp_lse_merge           exact log-sum-exp merge of the N partials
  * and, for moving a request prefilled without context sharding into the shards,
  *   5. dcp_kv_relayout         owner-filtered copy from a paged prefill pool
+ * and, on either side of the attention, the two absorption products
+ *   6. dcp_absorb_q            q_nope @ w_kc -> the 576-d absorbed query
+ *   7. dcp_absorb_o            merged latent output @ w_vc -> per-head value
  *
  * On one GPU the N context shards are N compact paged pools in one HBM
  * allocation (the "arena"), so the cross-rank steps (query all-gather,
@@ -297,6 +300,60 @@ int32_t dcp_mla_decode_partial_static(const dcp_layout_t* layout, int32_t shard_
 
 /* Size in bytes of the built-in scratch array dcp_mla_decode_partial_static uses. */
 size_t dcp_mla_decode_static_scratch_bytes(void);
+
+/*
+ * dcp_absorb_q — the query-side absorption product (identity 1).
+ *
+ * Sources: "MLA 的 Decode Context Parallelism", section 2 (identity 1: the K
+ * up-projection moves into the query, q_hat_h = q^C W^UK_h in R^512, and the
+ * decode query of head h is [q_hat_h || q^R_h], 576 dims); "Decode Context
+ * Parallelism" (zdszero), section "decode 路径：以 Kimi K3 的 MLA 为例"
+ * (w_kc [H, 128, 512] from the K part of kv_b_proj; bmm(q_nope, w_kc) ->
+ * [B, H, 512]; q_pe enters attention unrotated).
+ *
+ *   T            query tokens (B x q_len; row t = b * q_len + i)
+ *   q_nope       bf16, row (t, h) at element (t * H + h) * q_nope_stride; its
+ *                first 128 elements are read.  q_nope_stride >= 128 and a
+ *                multiple of 8 (a q_b_proj output [T, H, 192] passes its base
+ *                with stride 192).
+ *   q_pe         bf16, row (t, h) at (t * H + h) * q_pe_stride; 64 elements
+ *                read; q_pe_stride >= 64, a multiple of 8.
+ *   w_kc         bf16 [H, 128, 512]
+ *   q     (out)  bf16 [T, H, 576]: dims [0, 512) = q_nope[t, h] @ w_kc[h]
+ *                (f32 accumulation, rounded to nearest bf16), dims [512, 576)
+ *                = q_pe[t, h] unchanged.  This is the `q` operand of
+ *                dcp_mla_decode_partial.  Must not overlap the inputs.
+ *   status       device word (may be NULL); DCP_STATUS_TIMEOUT if a pipeline
+ *                wait gave up (q is then invalid).
+ * Every pointer must be 16-byte aligned.  T == 0 is a no-op.  Errors:
+ * DCP_ERR_INVALID on T < 0, H < 1 or H > 65535, more than 65535 tiles of 128
+ * tokens, a null or misaligned pointer, or a bad stride.
+ */
+int32_t dcp_absorb_q(int64_t T, int32_t H, const void* q_nope, int64_t q_nope_stride, const void* q_pe,
+                     int64_t q_pe_stride, const void* w_kc, void* q, int32_t* status, void* stream);
+
+/*
+ * dcp_absorb_o — the output-side absorption product (identity 2).
+ *
+ * Sources: "MLA 的 Decode Context Parallelism", section 2 (identity 2: the
+ * attention-weighted sum of W^UV_h c_t equals W^UV_h applied once to the
+ * weighted sum of latent rows); "Decode Context Parallelism" (zdszero),
+ * section "decode 路径：以 Kimi K3 的 MLA 为例" (w_vc [H, 512, 128] from the
+ * V part of kv_b_proj; bmm(O, w_vc) -> [B, H, 128] after the merge).
+ *
+ *   o            [T, H, 512] f32 or bf16 (o_dtype): the merged latent output
+ *                (dcp_lse_merge's `o` with rows = T * H).  An f32 o is rounded
+ *                to nearest bf16 in the kernel before the product (the tensor
+ *                core multiplies bf16 by bf16).
+ *   w_vc         bf16 [H, 512, 128]
+ *   v     (out)  [T, H, 128] f32 or bf16 (v_dtype): v[t, h] = o[t, h] @ w_vc[h],
+ *                f32 accumulation.  Must not overlap the inputs.
+ *   status       device word (may be NULL); DCP_STATUS_TIMEOUT as above.
+ * Every pointer must be 16-byte aligned.  T == 0 is a no-op.  Errors:
+ * DCP_ERR_INVALID as for dcp_absorb_q, or a bad dtype.
+ */
+int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_dtype, const void* w_vc, void* v,
+                     int32_t v_dtype, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
-              "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_kv_relayout"]:
+              "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_kv_relayout", "dcp_absorb_q",
+              "dcp_absorb_o"]:
         assert n in names
 
 
@@ -115,6 +116,33 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.dcp_lse_merge(0, 10, P(256), 0, P(256), 0, P(256), 0, P(256), None) == -1
     assert lib.dcp_lse_merge(2, 10, P(256), 3, P(256), 0, P(256), 0, P(256), None) == -1
     assert lib.dcp_lse_merge(2, 0, None, 0, None, 0, None, 0, None, None) == 0
+    # absorption products
+    aq = lambda **kw: dict(dict(T=4, H=8, qn=P(256), sn=192, qp=P(512), sp=192, w=P(1024), q=P(2048)), **kw)
+
+    def absorb_q(**kw):
+        a = aq(**kw)
+        return lib.dcp_absorb_q(a["T"], a["H"], a["qn"], a["sn"], a["qp"], a["sp"], a["w"], a["q"], None, None)
+    assert absorb_q(T=0) == 0                       # no-op, nothing launched
+    assert absorb_q(T=-1) == -1
+    assert absorb_q(H=0) == -1
+    assert absorb_q(H=70000) == -1
+    assert absorb_q(T=128 * 65536) == -1            # more token tiles than a grid dimension holds
+    assert absorb_q(sn=100) == -1                   # shorter than the 128 dims read
+    assert absorb_q(sn=196) == -1                   # not a multiple of 8 elements
+    assert absorb_q(sp=60) == -1
+    assert absorb_q(qn=P(264)) == -1                # not 16-byte aligned
+    assert absorb_q(w=None) == -1
+    assert absorb_q(q=None) == -1
+
+    def absorb_o(T=4, H=8, o=P(256), od=0, w=P(512), v=P(1024), vd=1):
+        return lib.dcp_absorb_o(T, H, o, od, w, v, vd, None, None)
+    assert absorb_o(T=0) == 0
+    assert absorb_o(od=2) == -1
+    assert absorb_o(vd=-1) == -1
+    assert absorb_o(T=0, od=5) == -1                # dtypes are checked even for an empty call
+    assert absorb_o(o=None) == -1
+    assert absorb_o(v=P(1032)) == -1
+    assert absorb_o(H=0) == -1
 
 
 def test_package_fails_loudly_without_library(monkeypatch, tmp_path):

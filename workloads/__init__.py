@@ -136,6 +136,24 @@ def gen_q(cfg: Config, device="cpu") -> torch.Tensor:
     return q.to(torch.bfloat16)
 
 
+def gen_q_proj(cfg: Config, device="cpu") -> torch.Tensor:
+    """Per-head query projection [B, q_len, H, 192] bf16 from N(0,1): dims [0, 128)
+    are q_nope, dims [128, 192) are q_pe (the input of the query-side absorption)."""
+    g = _gen(device, cfg.seed * 1000003 + 29)
+    q = torch.randn(cfg.B, cfg.q_len, cfg.H, 192, generator=g, device=device, dtype=torch.float32)
+    return q.to(torch.bfloat16)
+
+
+def gen_absorb_weights(cfg: Config, device="cpu"):
+    """Synthetic (w_kc [H, 128, 512], w_vc [H, 512, 128]) bf16 with entries drawn
+    from N(0, 1/fan_in) (fan_in 128 and 512), so q_nope @ w_kc has unit-variance
+    dims like the other query recipes and o @ w_vc stays on the scale of o."""
+    g = _gen(device, cfg.seed * 1000003 + 31)
+    w_kc = torch.randn(cfg.H, 128, DV, generator=g, device=device, dtype=torch.float32) / math.sqrt(128.0)
+    w_vc = torch.randn(cfg.H, DV, 128, generator=g, device=device, dtype=torch.float32) / math.sqrt(512.0)
+    return w_kc.to(torch.bfloat16), w_vc.to(torch.bfloat16)
+
+
 def gen_kv(cfg: Config, b: int, S_b: int, device="cpu") -> torch.Tensor:
     """Latent rows [S_b, 576] bf16 of request b in position order, from N(0,1)."""
     g = _gen(device, cfg.seed * 1000003 + 1009 * (b + 1))
