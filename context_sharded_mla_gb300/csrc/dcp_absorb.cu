@@ -107,7 +107,23 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   const int h = blockIdx.y;
   const int64_t t0 = (int64_t)blockIdx.z * kTokTile;
 
-  if (tid == 0) {
+  // One K-step of loads into stage ks % STAGES (producer thread only).
+  auto issue_loads = [&](int ks) {
+    const int s = ks % STAGES;
+    uint8_t* st = smem + s * L::kStage;
+    mbar_arrive_expect_tx(&full[s], (kAF32 ? 0u : kATileBytes) + kNBoxes * kWBoxBytes);
+    if (!kAF32) tma_load_3d(st, &tmap_a, &full[s], ks * kKStep, h, (int32_t)t0);
+#pragma unroll
+    for (int j = 0; j < kNBoxes; ++j)
+      tma_load_3d(st + kATileBytes + j * kWBoxBytes, &tmap_w, &full[s], n0 + 64 * j, ks * kKStep, h);
+  };
+
+  // The producer initialises the barriers and puts the first STAGES K-steps in
+  // flight at once, so their memory latency overlaps the TMEM allocation and
+  // the CTA barrier below.
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_w);
+    if (!kAF32) prefetch_tmap(&tmap_a);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], kAF32 ? 1 + 4 : 1);   // producer (+ one arrival per converting warp)
       mbar_init(&empty[s], 1);
@@ -115,6 +131,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     mbar_init(done, 1);
     *abort_s = 0;
     fence_barrier_init();
+    for (int ks = 0; ks < STAGES && ks < KSTEPS; ++ks) issue_loads(ks);
   }
   if (warp == kIssuerWarp) {
     tmem_alloc(tmem_slot, NT);
@@ -128,17 +145,9 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&tmap_w);
-      if (!kAF32) prefetch_tmap(&tmap_a);
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int s = ks % STAGES;
-        if (ks >= STAGES && !mbar_wait(&empty[s], ((ks / STAGES) - 1) & 1, abort_s)) break;
-        uint8_t* st = smem + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], (kAF32 ? 0u : kATileBytes) + kNBoxes * kWBoxBytes);
-        if (!kAF32) tma_load_3d(st, &tmap_a, &full[s], ks * kKStep, h, (int32_t)t0);
-#pragma unroll
-        for (int j = 0; j < kNBoxes; ++j)
-          tma_load_3d(st + kATileBytes + j * kWBoxBytes, &tmap_w, &full[s], n0 + 64 * j, ks * kKStep, h);
+      for (int ks = STAGES; ks < KSTEPS; ++ks) {
+        if (!mbar_wait(&empty[ks % STAGES], ((ks / STAGES) - 1) & 1, abort_s)) break;
+        issue_loads(ks);
       }
     }
   } else if (warp == kIssuerWarp) {
@@ -168,6 +177,16 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     const int row = tid;                        // this thread's token within the tile
     const int64_t t = t0 + row;
     bool ok = true;
+    if (kQuery && n0 == 0 && t < a.T) {
+      // the rope dims pass through: copy them while the product runs
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_pe + (t * a.H + h) * a.q_pe_stride);
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (t * a.H + h) * kDk + kDv);
+      uint4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __ldg(src + i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = x[i];
+    }
     if (kAF32) {
       // Convert A to bf16 into the swizzled K-major stage layout: 16-byte chunk c
       // of row r sits at r * 128 + ((c ^ (r % 8)) * 16) (tile base 1024-aligned).
@@ -203,38 +222,59 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     tc_fence_after();
     const bool warp_live = t0 + 32 * warp < a.T;   // warp-uniform: any of this warp's tokens exist
     if (ok && warp_live) {
+      // TMEM -> registers -> this thread's row of a staging tile in the (now
+      // idle) operand stages.  Rows are padded by 16 bytes so the eight threads
+      // of a store phase hit different banks.
+      const bool out_bf16 = kQuery || a.out_bf16;
+      const uint32_t row_bytes = NT * (out_bf16 ? 2 : 4);
+      const uint32_t srow = smem_u32(smem) + row * (row_bytes + 16);
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
       const bool live = t < a.T;
-#pragma unroll 1
-      for (int c = 0; c < NT / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + 32 * c, r);
-        tmem_ld_wait();
-        if (!live) continue;
-        if (kQuery || a.out_bf16) {
-          uint4 pk[4];
+      auto stage_chunk = [&](int c, const uint32_t (&r)[32]) {
+        if (!live) return;
+        if (out_bf16) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            pk[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1])),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
-          const int64_t width = kQuery ? kDk : 128;
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (t * a.H + h) * width +
-                                                n0 + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+            st_shared_v4(srow + 64 * c + 16 * i,
+                         pack_bf16x2(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.out) + (t * a.H + h) * 128 + n0 + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(srow + 128 * c + 16 * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
         }
+      };
+      // Two register buffers: the TMEM load of the next 32 columns is in flight
+      // while the current ones are converted and staged.  NT / 32 is even.
+      uint32_t ra[32], rb[32];
+      tmem_ld32(lane_addr, ra);
+#pragma unroll 1
+      for (int c = 0; c < NT / 32; c += 2) {
+        tmem_ld_wait_regs(ra);
+        tmem_ld32(lane_addr + 32 * (c + 1), rb);
+        stage_chunk(c, ra);
+        tmem_ld_wait_regs(rb);
+        if (c + 2 < NT / 32) tmem_ld32(lane_addr + 32 * (c + 2), ra);
+        stage_chunk(c + 1, rb);
       }
-      if (kQuery && n0 == 0 && live) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.q_pe + (t * a.H + h) * a.q_pe_stride);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (t * a.H + h) * kDk + kDv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = __ldg(src + i);
+      // The warp then writes its own 32 staged rows out, one row segment per
+      // coalesced store (16 bytes per lane).
+      __syncwarp();
+      const int64_t width = kQuery ? kDk : 128;
+      const uint32_t esz = out_bf16 ? 2 : 4;
+      const uint32_t lanes_per_row = row_bytes / 16;            // 32 or 16
+      const int rows_per_iter = 32 / lanes_per_row;              // 1 or 2
+      const int sub = lane / lanes_per_row, col16 = lane % lanes_per_row;
+#pragma unroll 4
+      for (int j = sub; j < 32; j += rows_per_iter) {
+        const int rr = 32 * warp + j;
+        const int64_t tt = t0 + rr;
+        if (tt >= a.T) break;                                    // rows are in order: the rest are past T
+        const uint4 x = ld_shared_v4(smem_u32(smem) + rr * (row_bytes + 16) + 16 * col16);
+        uint8_t* g = reinterpret_cast<uint8_t*>(a.out) + ((tt * a.H + h) * width + n0) * esz + 16 * col16;
+        *reinterpret_cast<uint4*>(g) = x;
       }
     }
   }
@@ -344,9 +384,9 @@ extern "C" int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_d
   a.status = status;
   if (o_dtype == DCP_BF16) {
     if (!make_tmap_a(&ta, o, kDv, H, T, kDv)) return DCP_ERR_CUDA;
-    return launch<128, 8, 4, false, false>(ta, tw, a, 1, as_stream(stream));
+    return launch<128, 8, 6, false, false>(ta, tw, a, 1, as_stream(stream));
   }
   a.a_f32 = reinterpret_cast<const float*>(o);
   a.a_f32_stride = kDv;
-  return launch<128, 8, 4, false, true>(tw, tw, a, 1, as_stream(stream));
+  return launch<128, 8, 6, false, true>(tw, tw, a, 1, as_stream(stream));
 }
