@@ -86,6 +86,7 @@ constexpr int kProducerWarp = 10;
 constexpr int kMmaWarp = 11;                  // QK issuer and TMEM owner
 constexpr int kPvWarp = 9;                    // PV issuer
 constexpr int kMaxGroupRows = 128;
+constexpr int64_t kMaxQueryRows = 65536;      // q_len * H per request (512 row groups)
 constexpr uint32_t kOCol = 0;                 // TMEM columns [0, 256): O, rows on lanes
 constexpr uint32_t kSCol = 256;               // [256, 384): two S tiles of 64 fp32 columns
 constexpr uint32_t kPCol = 384;               // [384, 448): P of two tiles as bf16 pairs (2 x 32)
@@ -1173,15 +1174,27 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   // clusters that can be resident at once (both CTAs of a cluster share a GPC)
   const int clusters = max_active_clusters(p->smem);
   if (clusters > 0) {
-    p->V = clusters / p->ngroups;
-    if (p->V < 1) p->V = 1;
+    // V ranges per row group.  One wave of V0 = clusters / ngroups ranges is the
+    // default; when that leaves many clusters idle (ngroups not much below the
+    // cluster count, e.g. a chunked extend's many row groups), a larger V run
+    // in several waves finishes sooner: the time is waves / V of one group's
+    // whole sequence.  A larger V must gain 5 % to pay for its cut units.
+    const int V0 = clusters / p->ngroups > 1 ? clusters / p->ngroups : 1;
+    auto cost = [&](int Vc) {
+      return (double)(((int64_t)Vc * p->ngroups + clusters - 1) / clusters) / Vc;
+    };
+    int best = V0;
+    for (int Vc = V0 + 1; Vc <= 8; ++Vc)
+      if (cost(Vc) < 0.95 * cost(best)) best = Vc;
+    p->V = best;
   }
   const int P = layout->page_size;
   p->box_rows = P >= kTile ? kTile : P;
   const int64_t U = (int64_t)B * n_held;
   p->ws_start_bytes = align256((size_t)(U + 1) * 4);
-  p->ws_piece_o_bytes = align256((size_t)2 * p->V * R_total * kDv * 4);
-  p->ws_piece_lse_bytes = align256((size_t)2 * p->V * R_total * 4);
+  // With one range per row group no unit is cut, so no piece is ever written.
+  p->ws_piece_o_bytes = p->V > 1 ? align256((size_t)2 * p->V * R_total * kDv * 4) : 0;
+  p->ws_piece_lse_bytes = p->V > 1 ? align256((size_t)2 * p->V * R_total * 4) : 0;
   p->ws_total = p->ws_start_bytes + p->ws_piece_o_bytes + p->ws_piece_lse_bytes;
   return nts >= 3;
 }
@@ -1222,7 +1235,7 @@ bool page_size_ok(int P) { return P >= 8 && P % 8 == 0 && (P % kTile == 0 || kTi
 extern "C" size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int32_t shard_begin,
                                                 int32_t shard_end, int32_t B, int32_t q_len, int32_t H) {
   if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end ||
-      B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > 1024)
+      B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > kMaxQueryRows)
     return 0;
   Plan p;
   if (!make_plan(layout, shard_end - shard_begin, B, q_len, H, &p)) return 0;
@@ -1239,7 +1252,7 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
                                           int32_t* status, void* stream) {
   if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end)
     return DCP_ERR_INVALID;
-  if (B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > 1024) return DCP_ERR_INVALID;
+  if (B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > kMaxQueryRows) return DCP_ERR_INVALID;
   if (pool_pages < 1 || max_pages < 1 || bt_stride < max_pages) return DCP_ERR_INVALID;
   if (!q || !arena || !block_table || !seq_lens || !o_part || !lse_part) return DCP_ERR_INVALID;
   if (o_part_dtype != DCP_F32 && o_part_dtype != DCP_BF16) return DCP_ERR_INVALID;

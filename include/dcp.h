@@ -228,7 +228,11 @@ int32_t dcp_kv_relayout(const dcp_layout_t* layout, int32_t shard_begin, int32_t
  *              and are meaningless after the call
  * Rows of a page past the request's length are read but carry zero weight;
  * they must hold finite values (a zero-initialised pool and dcp_kv_append
- * guarantee that).  Supported: 1 <= H, q_len * H <= 1024, B >= 1.
+ * guarantee that).  Supported: 1 <= H, q_len * H <= 65536, B >= 1.  A large
+ * q_len is a chunked extend in the all-gather-Q form: the chunk's query tokens
+ * attend to every shard's rows exactly as decode tokens do, causally in global
+ * positions (vLLM-Ascend "上下文并行（CP）", chunked prefill: the work after
+ * gathering Q is the decode work).
  * Errors: DCP_ERR_INVALID on bad sizes/pointers/dtype/base, DCP_ERR_WORKSPACE
  * if the workspace is too small.  Device status: BAD_LENGTH, BAD_PAGE_ID.
  */

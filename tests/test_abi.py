@@ -71,7 +71,7 @@ def test_host_validation_rejects_bad_arguments(lib):
                             P(16), None) == 0       # T == 0 is a no-op
     assert lib.dcp_kv_append(ctypes.byref(good), 0, 5, P(16), P(16), P(16), 1, P(16), 1, P(16), None) == -1
     assert lib.dcp_kv_append(ctypes.byref(good), 0, 4, P(17), P(16), P(16), 1, P(16), 1, P(16), None) == -1
-    # decode: H*q_len over the limit, bad base, bad dtype, missing workspace
+    # decode: q_len*H over the limit, bad base, bad dtype, missing workspace
     args = lambda **kw: dict(dict(sb=0, se=4, q=P(256), B=1, ql=1, H=16, ar=P(256), pp=1, bt=P(256), st=1, mp=1,
                                   sl=P(256), sc=0.1, base=0, op=P(256), od=0, lp=P(256), ws=None, wsb=0,
                                   status=P(256)), **kw)
@@ -81,7 +81,8 @@ def test_host_validation_rejects_bad_arguments(lib):
         return lib.dcp_mla_decode_partial(ctypes.byref(good), a["sb"], a["se"], a["q"], a["B"], a["ql"], a["H"],
                                           a["ar"], a["pp"], a["bt"], a["st"], a["mp"], a["sl"], a["sc"], a["base"],
                                           a["op"], a["od"], a["lp"], a["ws"], a["wsb"], a["status"], None)
-    assert call(H=2048) == -1
+    assert call(H=65537) == -1                      # more than 65536 query rows per request
+    assert call(ql=512, H=129) == -1
     assert call(base=7) == -1
     assert call(od=9) == -1
     assert call(sc=-1.0) == -1

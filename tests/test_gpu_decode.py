@@ -2,8 +2,9 @@
 
 Sizes are small enough for the oracle to finish in seconds but span several
 KV tiles per shard and a ragged tail; every workload family is covered
-(token RR and interleave 16, base e and base 2, q_len 1 and causal q_len 4,
-fp32 and bf16 partials), plus empty shards, needles and the merge alone.
+(token RR and interleave 16, base e and base 2, q_len 1, causal q_len 4 and
+the 64-token chunked extend, fp32 and bf16 partials), plus empty shards,
+needles and the merge alone.
 Tolerance (written here, from the stated bar): |err| <= 1e-2 + 1e-2 |ref| for
 outputs, 1e-3 absolute for lse.
 """
@@ -53,6 +54,7 @@ SMALL = {
     "k3": dict(B=3, S=4096 + 13),
     "ragged": dict(B=5, S=3000, S_min=17),
     "long": dict(B=2, S=20000 + 7),
+    "extend": dict(B=2, S=3000 + 5, H=32),   # 64 causal query tokens x 32 heads = 16 row groups
 }
 
 
@@ -225,3 +227,19 @@ def test_bad_length_sets_status():
     st.seq_lens.fill_(1)            # shorter than q_len
     st.decode()
     assert st.dec.status_bits() & 16
+
+
+def test_extend_more_row_groups_than_clusters():
+    """80 causal query tokens x 128 heads = 80 row groups of 128 rows: more groups
+    than resident clusters, so one stream-K range per group (no pieces)."""
+    cfg = workloads.config("extend", B=2, H=128, q_len=80, S=1500, N=8)
+    st = GpuState(cfg)
+    _check_state(st, heads=[0, 1, 64, 127])
+
+
+def test_extend_chunk_across_shard_boundaries():
+    """A 200-token chunk with interleave 16 over 4 shards: query rows straddle
+    several owner blocks, early rows see fewer shards' tokens."""
+    cfg = workloads.config("extend", B=1, H=8, q_len=200, S=1000 + 3, N=4, I=16, P=64)
+    st = GpuState(cfg)
+    _check_state(st)

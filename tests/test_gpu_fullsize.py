@@ -22,6 +22,7 @@ SAMPLES = {
     "k3": dict(reqs=[0, 63], heads=None),
     "ragged": dict(reqs=None, heads=list(range(0, 128, 4))),
     "long": dict(reqs=[0], heads=None),
+    "extend": dict(reqs=[3], heads=[0, 95]),
 }
 
 

@@ -12,6 +12,8 @@ queries from N(0,1), softmax scale 1/sqrt(192), shuffled block tables):
   k3      B=64,  H=96,  q_len=1, S=131072, +1-token append, N=8, I=1, P=64, base 2
   ragged  B=128, H=128, q_len=4 (causal), S_b log-uniform in [1024, 262144], N=16, I=16, P=64, base e
   long    B=4,   H=96,  q_len=1, S=1048576, +8192-token chunk append at a=S-8192, N=8, I=1, P=64, base e
+  extend  B=4,   H=96,  q_len=64 (causal), S=131072, +64-token chunk append, N=8, I=1, P=64, base e
+          (a chunked extend in the all-gather-Q form: the chunk's 64 tokens are the query rows)
 
 Capacity: the pool is sized with the widened-page rule of the SGLang page
 "Decode context parallelism" ("Virtual KV layout"): one virtual page covers
@@ -42,6 +44,8 @@ _BASE = {
                    out_dtype="bf16", seed=4, append=0, chunk=0, ragged=True),
     "long": dict(B=4, H=96, q_len=1, S=1048576, N=8, I=1, P=64, base=0, out_dtype="bf16",
                  seed=5, append=0, chunk=8192, ragged=False),
+    "extend": dict(B=4, H=96, q_len=64, S=131072, N=8, I=1, P=64, base=0, out_dtype="bf16",
+                   seed=6, append=0, chunk=64, ragged=False),
 }
 
 DESCRIPTIONS = {
@@ -50,6 +54,8 @@ DESCRIPTIONS = {
     "k3": "K3-shaped: B=64 H=96 S=131072 N=8 RR page64 base-2 +1-token owner-filtered append",
     "ragged": "ragged verify: B=128 H=128 q_len=4 causal S~logU[1k,256k] N=16 I=16 page64 base-e",
     "long": "long context: B=4 H=96 S=1048576 N=8 RR page64 base-e +8192-token chunk append",
+    "extend": "chunked extend (all-gather-Q): B=4 H=96 q_len=64 causal S=131072 N=8 RR page64 base-e "
+              "+64-token chunk append",
 }
 
 
