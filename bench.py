@@ -275,7 +275,7 @@ def run_ours(args, cfg, rank, world, dist, device):
     else:
         roof = {"bound": "tensor", "achieved": round(part_flops, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(part_flops / peaks["bf16_tflops"], 4)}
-    roof["traffic"] = recorded_traffic(cfg)
+    roof["traffic"] = recorded_traffic(cfg.name) if args.batch is None else None
     roof["kernel"] = "dcp_mla_decode_partial (all its launches, CUDA events on the launching stream)"
     roof["peak_source"] = f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured" else "fallback"
     result = {
@@ -559,7 +559,9 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
         "kernels_us": {"absorb_q": round(q_ms * 1e3, 3), "absorb_o": round(o_ms * 1e3, 3)},
         "bytes_alg": {"absorb_q": q_bytes, "absorb_o": o_bytes},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": (recorded_traffic("absorb_q") if q_ms >= o_ms and cfg.name == "k3"
+                                 and args.batch is None else None),
                      "kernel": f"{dom[0]} (CUDA events on the launching stream)",
                      "peak_source": f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured"
                      else "fallback"},
@@ -645,8 +647,8 @@ def run_e2e(args, cfg, st, dist, acct):
             "steps": n, "path": "ShardedMlaDecoder.step over the C ABI, pinned host buffers"}
 
 
-def recorded_traffic(cfg):
-    """DRAM bytes per launch of the partial from a committed ncu summary, if it matches this source."""
+def recorded_traffic(key):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if it matches the current source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -654,10 +656,12 @@ def recorded_traffic(cfg):
         with open(path) as f:
             rec = json.load(f)
         import hashlib
-        src = os.path.join(ROOT, "context_sharded_mla_gb300", "csrc", "dcp_decode.cu")
+        entry = rec.get(key)
+        if not entry:
+            return None
+        src = os.path.join(ROOT, entry.get("source", "context_sharded_mla_gb300/csrc/dcp_decode.cu"))
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        entry = rec.get(cfg.name)
-        if not entry or entry.get("source_sha") != h:
+        if entry.get("source_sha") != h:
             return None
         scale = entry.get("scale_to_full", 1.0)
         return int(entry["dram_bytes_per_launch"] * scale)
