@@ -50,6 +50,12 @@ constexpr int kKStep = 64;                    // K elements per pipeline stage
 constexpr int kTokTile = 128;                 // tokens per CTA (MMA M)
 constexpr uint32_t kATileBytes = kTokTile * kKStep * 2;   // 16 KB
 constexpr uint32_t kWBoxBytes = kKStep * 64 * 2;          // one [64 k][64 n] box, 8 KB
+// Output columns per CTA.  Narrower tiles (128 / 64 columns: 4 / 2 CTAs per
+// head, 3 / 2 CTAs per SM) measured 12 % / 9 % slower at the K3 shapes: more
+// CTAs start later and re-read the activations.
+constexpr int kQTile = 256;                   // query side: 2 CTAs per head, 96 KB shared each
+constexpr int kOTile = 128;                   // output side: 1 CTA per head
+constexpr int kOStages = 6;                   // output side: 6 of its 8 K-steps in flight, 192 KB shared
 
 template <int NT, int KSTEPS, int STAGES>
 struct AbsorbSmem {
@@ -363,7 +369,7 @@ extern "C" int32_t dcp_absorb_q(int64_t T, int32_t H, const void* q_nope, int64_
   a.q_pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
   a.q_pe_stride = q_pe_stride;
   a.status = status;
-  return launch<256, 2, 2, true, false>(ta, tw, a, kDv / 256, as_stream(stream));
+  return launch<kQTile, 2, 2, true, false>(ta, tw, a, kDv / kQTile, as_stream(stream));
 }
 
 extern "C" int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_dtype, const void* w_vc, void* v,
@@ -384,9 +390,9 @@ extern "C" int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_d
   a.status = status;
   if (o_dtype == DCP_BF16) {
     if (!make_tmap_a(&ta, o, kDv, H, T, kDv)) return DCP_ERR_CUDA;
-    return launch<128, 8, 6, false, false>(ta, tw, a, 1, as_stream(stream));
+    return launch<kOTile, 8, kOStages, false, false>(ta, tw, a, 128 / kOTile, as_stream(stream));
   }
   a.a_f32 = reinterpret_cast<const float*>(o);
   a.a_f32_stride = kDv;
-  return launch<128, 8, 6, false, true>(tw, tw, a, 1, as_stream(stream));
+  return launch<kOTile, 8, kOStages, false, true>(tw, tw, a, 128 / kOTile, as_stream(stream));
 }
