@@ -981,6 +981,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   }
+  else if (warp < 8) {
+    // No rows of the group: zero this warp's 16 TMEM lanes of the P and query
+    // columns once, so the M = 128 products carry zeros, not stale data, in the
+    // padding rows (their results are never read).
+    const uint32_t zl = (uint32_t)(32 * (warp & 3) + kHalfRows * (warp >> 2)) << 16;
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    tmem_st16x2<32>(tmem + zl + kPCol, z);
+    tmem_st16x2<32>(tmem + zl + kQCol, z);
+    tmem_st_wait();
+  }
 
   if (*abort_s && tid == 0) flag(a.status, DCP_STATUS_TIMEOUT);
   tc_fence_before();
