@@ -35,7 +35,7 @@ DCP_ERR_TOO_LARGE = -5
 DCP_LSE_BASE_E, DCP_LSE_BASE_2 = 0, 1
 DCP_F32, DCP_BF16 = 0, 1
 STATUS_BITS = {1: "BAD_POSITION", 2: "BAD_PAGE_INDEX", 4: "BAD_PAGE_ID", 8: "BAD_REQUEST", 16: "BAD_LENGTH",
-               32: "TIMEOUT"}
+               32: "TIMEOUT", 64: "INTERNAL"}
 
 
 class DcpError(RuntimeError):

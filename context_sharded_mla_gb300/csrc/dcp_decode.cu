@@ -128,11 +128,13 @@ __host__ __device__ inline uint32_t round1024(uint32_t v) { return (v + 1023u) &
 
 __host__ __device__ inline SmemLayout smem_layout(int Rg, int nts) {
   SmemLayout s;
-  // The M = 128 shared-memory A operands hold only the group's Rg rows; the
-  // products also read the 128 - Rg rows that follow (whatever lies there) into
-  // TMEM lanes no thread reads back.
-  s.qc = 0;                                        // query chunks 4r + 2, 4r + 3: [Rg][64] bf16 each, 128-byte swizzle
-  s.qr = 2 * (uint32_t)Rg * 128;                   // query rope dims [32r, 32r + 32): [Rg][32], 64-byte swizzle
+  // The M = 128 shared-memory A operands hold the group's Rg rows; the products
+  // also read the 128 - Rg rows that follow into TMEM lanes no thread reads
+  // back.  Query chunk 4r + 2 is given all 128 rows, zeroed, so its padding
+  // rows multiply zeros (less power at the power cap); chunk 4r + 3 and the
+  // rope dims are followed by other data, as the ring needs the space.
+  s.qc = 0;                                        // query chunks 4r + 2 ([128][64], rows >= Rg zero), 4r + 3 ([Rg][64]), bf16, 128-byte swizzle
+  s.qr = (128 + (uint32_t)Rg) * 128;               // query rope dims [32r, 32r + 32): [Rg][32], 64-byte swizzle
   s.x = round1024(s.qr + (uint32_t)Rg * 64);       // two [Rg][64] fp32 buffers: partial scores staged / received
   s.xbuf = round1024((uint32_t)Rg * kXRowBytes);
   s.ring = s.x + 2 * s.xbuf;                       // tile slots: 4 value chunks + this CTA's rope half
@@ -406,8 +408,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_q64, const __grid_constant__ CUtensorMap tmap_kv64,
                       const __grid_constant__ CUtensorMap tmap_kv4, TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The layout needs a 1024-byte aligned base and the launch reserves no slack
+  // for aligning it here: every CTA of the launch sees the same base, so a
+  // misaligned one makes all of them stop at once, before any barrier.
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) flag(a.status, DCP_STATUS_INTERNAL);
+    return;
+  }
+  unsigned char* smem = smem_raw;
   const SmemLayout sl = smem_layout(a.Rg, a.nts);
   unsigned char* qc_s = smem + sl.qc;
   unsigned char* qr_s = smem + sl.qr;
@@ -619,7 +627,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int32_t qy = b * a.R_total + g * Rg;
           mbar_arrive_expect_tx(&bars[kQFull], Rg * (2 * 128 + 64));
           for (int i = kQTmemChunks; i < kOwnChunks; ++i)
-            tma_load_2d(qc_s + (i - kQTmemChunks) * Rg * 128, &tmap_q, &bars[kQFull],
+            tma_load_2d(qc_s + (i - kQTmemChunks) * 128 * 128, &tmap_q, &bars[kQFull],
                         (kOwnChunks * (int)rank + i) * kChunkDims, qy);
           tma_load_2d(qr_s, &tmap_q64, &bars[kQFull], 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, qy);
         }
@@ -693,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = kQTmemChunks; i < kOwnChunks; ++i)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, qcdesc0 + (i - kQTmemChunks) * ((Rg * 128) >> 4) + 2 * kk,
+            mma_bf16_ss(d, qcdesc0 + (i - kQTmemChunks) * ((128 * 128) >> 4) + 2 * kk,
                         kd + i * (kChunkBytes >> 4) + 2 * kk, idesc_qk, 1);
 #pragma unroll
         for (int kk = 0; kk < kRopeHalf / 16; ++kk) mma_bf16_ss(d, qrdesc0 + 2 * kk, rdesc0 + soff + 2 * kk, idesc_qk, 1);
@@ -1178,11 +1186,11 @@ bool make_plan(const dcp_layout_t* layout, int n_held, int B, int q_len, int H, 
   p->V = (sms / 2) / p->ngroups;  // ranges: one 2-CTA cluster per (range, row group)
   if (p->V < 1) p->V = 1;
   const SmemLayout base = smem_layout(p->Rg, 0);
-  const size_t budget = 232448 - 1024;  // 227 KB minus alignment slack
+  const size_t budget = 232448;  // 227 KB
   int nts = (int)((budget - base.total) / kSlotBytes);
   if (nts > kMaxTileSlots) nts = kMaxTileSlots;
   p->nts = nts;
-  p->smem = smem_layout(p->Rg, nts).total + 1024;
+  p->smem = smem_layout(p->Rg, nts).total;
   // clusters that can be resident at once (both CTAs of a cluster share a GPC)
   const int clusters = max_active_clusters(p->smem);
   if (clusters > 0) {

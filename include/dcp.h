@@ -79,7 +79,8 @@ enum {
   DCP_STATUS_BAD_PAGE_ID = 4,     /* block-table entry outside [0, pool_pages) */
   DCP_STATUS_BAD_REQUEST = 8,     /* request index outside [0, B) */
   DCP_STATUS_BAD_LENGTH = 16,     /* seq_len < q_len */
-  DCP_STATUS_TIMEOUT = 32         /* a kernel pipeline wait gave up (the call's outputs are invalid) */
+  DCP_STATUS_TIMEOUT = 32,        /* a kernel pipeline wait gave up (the call's outputs are invalid) */
+  DCP_STATUS_INTERNAL = 64        /* a kernel found its shared memory misaligned and did nothing (outputs invalid) */
 };
 
 enum { DCP_LSE_BASE_E = 0, DCP_LSE_BASE_2 = 1 };
