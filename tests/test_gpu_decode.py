@@ -231,10 +231,26 @@ def test_bad_length_sets_status():
 
 def test_extend_more_row_groups_than_clusters():
     """80 causal query tokens x 128 heads = 80 row groups of 128 rows: more groups
-    than resident clusters, so one stream-K range per group (no pieces)."""
+    than resident clusters (76 on GB300), run as several waves of stream-K ranges
+    with cut units merged by the fixup."""
     cfg = workloads.config("extend", B=2, H=128, q_len=80, S=1500, N=8)
     st = GpuState(cfg)
     _check_state(st, heads=[0, 1, 64, 127])
+
+
+def test_extend_one_range_per_row_group():
+    """76 tokens x 128 heads = 76 row groups: no larger range count gains on 76
+    clusters, so each group is one range, no unit is cut and no piece workspace
+    is reserved."""
+    import context_sharded_mla_gb300 as dcp
+    cfg = workloads.config("extend", B=2, H=128, q_len=76, S=1200, N=8)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        ws = dcp.dcp_mla_decode_workspace_size(dcp.Layout(cfg.N, cfg.I, cfg.P), 0, cfg.N, cfg.B, 76, 128)
+        assert 0 < ws < 4096            # tile starts only: no piece workspace
+        ws80 = dcp.dcp_mla_decode_workspace_size(dcp.Layout(cfg.N, cfg.I, cfg.P), 0, cfg.N, cfg.B, 80, 128)
+        assert ws80 > 80 * 128 * 512 * 4  # several ranges per group: pieces reserved
+    st = GpuState(cfg)
+    _check_state(st, heads=[0, 63, 127])
 
 
 def test_extend_chunk_across_shard_boundaries():
