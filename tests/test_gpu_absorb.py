@@ -15,7 +15,7 @@ import torch
 
 import workloads
 from oracle import absorb as oabsorb
-from tests.harness import GpuState, assert_close_o, bits, to_f64
+from harness import GpuState, assert_close_o, bits, to_f64
 
 pytestmark = pytest.mark.gpu
 

@@ -8,7 +8,6 @@ lengths).  Each replay is checked against the fp64 oracle over the cache as it
 stands after that append.
 """
 
-import numpy as np
 import pytest
 import torch
 
