@@ -259,3 +259,11 @@ def test_extend_chunk_across_shard_boundaries():
     cfg = workloads.config("extend", B=1, H=8, q_len=200, S=1000 + 3, N=4, I=16, P=64)
     st = GpuState(cfg)
     _check_state(st)
+
+
+def test_extend_at_the_row_limit():
+    """q_len * H = 512 x 128 = 65536 query rows, the largest a call takes: 512 row
+    groups in waves, causal over a 700-token cache of which 512 are the chunk."""
+    cfg = workloads.config("extend", B=1, H=128, q_len=512, S=700, N=4, P=16)
+    st = GpuState(cfg)
+    _check_state(st, heads=[0, 77, 127])
