@@ -138,6 +138,10 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
+        return self.summarize()
+
+    def summarize(self):
+        """Median / minimum SM clock and the throttle reasons seen between the marks."""
         import datetime
         lo, hi = (self.marks[0], self.marks[-1]) if len(getattr(self, "marks", [])) >= 2 else (None, None)
         sm, mx, reasons, all_sm = [], [], set(), []
