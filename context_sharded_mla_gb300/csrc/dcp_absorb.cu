@@ -323,17 +323,12 @@ bool make_tmap_w(CUtensorMap* m, const void* base, int64_t H, int64_t K, int64_t
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Raise the kernel's dynamic shared-memory limit once per instance.
+// Raise the kernel's dynamic shared-memory limit, once per instance and device.
 template <int NT, int KSTEPS, int STAGES, bool kQuery, bool kAF32>
 bool prepare() {
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [] {
-    ok = cudaFuncSetAttribute(absorb_kernel<NT, KSTEPS, STAGES, kQuery, kAF32>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)AbsorbSmem<NT, KSTEPS, STAGES>::kBytes) == cudaSuccess;
-  });
-  return ok;
+  static SmemLimit limit;
+  return limit.ensure(reinterpret_cast<const void*>(&absorb_kernel<NT, KSTEPS, STAGES, kQuery, kAF32>),
+                      AbsorbSmem<NT, KSTEPS, STAGES>::kBytes);
 }
 
 template <int NT, int KSTEPS, int STAGES, bool kQuery, bool kAF32>

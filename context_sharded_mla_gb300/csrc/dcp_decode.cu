@@ -1152,15 +1152,27 @@ int sm_count_current() {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+SmemLimit g_partial_smem;  // partial_tc_kernel's dynamic shared-memory limit, per device
+
+// Resident 2-CTA clusters of partial_tc_kernel at `smem` bytes on the current
+// device.  Cached per device and shared-memory size (a workload uses one or two
+// sizes); guarded by a mutex, since one host thread per GPU may plan at once.
 int max_active_clusters(size_t smem) {
-  static size_t cached_smem = 0;
-  static int cached = -1, cached_dev = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cached >= 0 && cached_smem == smem && cached_dev == dev) return cached;
-  if (cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return 0;
+  constexpr int kEntries = 8;
+  struct Entry {
+    size_t smem;
+    int clusters;
+  };
+  static std::mutex m;
+  static Entry cache[kMaxDevices][kEntries] = {};
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  {
+    std::lock_guard<std::mutex> lock(m);
+    for (const Entry& e : cache[dev])
+      if (e.smem == smem && e.clusters > 0) return e.clusters;
+  }
+  if (!g_partial_smem.ensure(reinterpret_cast<const void*>(&partial_tc_kernel), smem)) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 512, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1170,9 +1182,16 @@ int max_active_clusters(size_t smem) {
     cudaGetLastError();
     return 0;
   }
-  cached = n;
-  cached_smem = smem;
-  cached_dev = dev;
+  if (n > 0) {
+    std::lock_guard<std::mutex> lock(m);
+    Entry* slot = &cache[dev][0];
+    for (Entry& e : cache[dev])
+      if (e.clusters == 0 || e.smem == smem) {
+        slot = &e;
+        break;
+      }
+    *slot = Entry{smem, n};
+  }
   return n;
 }
 
@@ -1262,14 +1281,14 @@ extern "C" size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int3
   return p.ws_total;
 }
 
-extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
-                                          const void* q, int32_t B, int32_t q_len, int32_t H,
-                                          const void* arena, int64_t pool_pages,
-                                          const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
-                                          const int64_t* seq_lens, float scale, int32_t lse_base,
-                                          void* o_part, int32_t o_part_dtype, float* lse_part,
-                                          void* workspace, size_t workspace_bytes,
-                                          int32_t* status, void* stream) {
+namespace {
+
+// Host checks of dcp_mla_decode_partial's arguments (all but the workspace).
+int32_t check_decode_args(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end, const void* q,
+                          int32_t B, int32_t q_len, int32_t H, const void* arena, int64_t pool_pages,
+                          const int32_t* block_table, int64_t bt_stride, int64_t max_pages, const int64_t* seq_lens,
+                          float scale, int32_t lse_base, const void* o_part, int32_t o_part_dtype,
+                          const float* lse_part) {
   if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end)
     return DCP_ERR_INVALID;
   if (B < 1 || q_len < 1 || H < 1 || (int64_t)q_len * H > kMaxQueryRows) return DCP_ERR_INVALID;
@@ -1282,30 +1301,30 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
        reinterpret_cast<uintptr_t>(o_part)) & 15)
     return DCP_ERR_INVALID;
   if (!page_size_ok(layout->page_size)) return DCP_ERR_UNSUPPORTED;
+  const int64_t pool_rows = pool_pages * layout->page_size;
+  const int64_t n_held = shard_end - shard_begin;
+  if (n_held * pool_rows >= INT32_MAX || (int64_t)B * q_len * H >= INT32_MAX || (int64_t)B * n_held >= INT32_MAX / 2)
+    return DCP_ERR_UNSUPPORTED;
+  return DCP_OK;
+}
+
+// Tensor maps and the three launches of one partial decode on a checked plan and
+// a workspace of at least p.ws_total bytes (256-byte aligned).
+int32_t launch_decode(const Plan& p, const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                      const void* q, int32_t B, int32_t q_len, int32_t H, const void* arena, int64_t pool_pages,
+                      const int32_t* block_table, int64_t bt_stride, int64_t max_pages, const int64_t* seq_lens,
+                      float scale, int32_t lse_base, void* o_part, int32_t o_part_dtype, float* lse_part,
+                      void* workspace, int32_t* status, void* stream) {
   const int n_held = shard_end - shard_begin;
   const int64_t pool_rows = pool_pages * layout->page_size;
-  if ((int64_t)n_held * pool_rows >= INT32_MAX || (int64_t)B * q_len * H >= INT32_MAX ||
-      (int64_t)B * n_held >= INT32_MAX / 2)
-    return DCP_ERR_UNSUPPORTED;
-  Plan p;
-  if (!make_plan(layout, n_held, B, q_len, H, &p)) return DCP_ERR_CUDA;
-  if (!workspace || workspace_bytes < p.ws_total) return DCP_ERR_WORKSPACE;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255) return DCP_ERR_INVALID;
-
   CUtensorMap tq, tkv, tq64, tkv64, tkv4;
   if (!make_tmap(&tq, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg)) return DCP_ERR_CUDA;
   if (!make_tmap(&tkv, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
   if (!make_tmap(&tq64, q, (uint64_t)B * q_len * H, (uint32_t)p.Rg, true)) return DCP_ERR_CUDA;
   if (!make_tmap(&tkv64, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows, true)) return DCP_ERR_CUDA;
   if (!make_tmap_chunks(&tkv4, arena, (uint64_t)n_held * pool_rows, (uint32_t)p.box_rows)) return DCP_ERR_CUDA;
+  if (!g_partial_smem.ensure(reinterpret_cast<const void*>(&partial_tc_kernel), p.smem)) return DCP_ERR_CUDA;
 
-  static size_t smem_set = 0;
-  if (smem_set < p.smem) {
-    if (cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
-        cudaSuccess)
-      return DCP_ERR_CUDA;
-    smem_set = p.smem;
-  }
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   TcArgs a;
   a.L = to_layout(layout);
@@ -1336,6 +1355,29 @@ extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t sh
   return launch_status(3);
 }
 
+}  // namespace
+
+extern "C" int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
+                                          const void* q, int32_t B, int32_t q_len, int32_t H,
+                                          const void* arena, int64_t pool_pages,
+                                          const int32_t* block_table, int64_t bt_stride, int64_t max_pages,
+                                          const int64_t* seq_lens, float scale, int32_t lse_base,
+                                          void* o_part, int32_t o_part_dtype, float* lse_part,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* status, void* stream) {
+  const int32_t rc = check_decode_args(layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages,
+                                       block_table, bt_stride, max_pages, seq_lens, scale, lse_base, o_part,
+                                       o_part_dtype, lse_part);
+  if (rc != DCP_OK) return rc;
+  Plan p;
+  if (!make_plan(layout, shard_end - shard_begin, B, q_len, H, &p)) return DCP_ERR_CUDA;
+  if (!workspace || workspace_bytes < p.ws_total) return DCP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return DCP_ERR_INVALID;
+  return launch_decode(p, layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages, block_table, bt_stride,
+                       max_pages, seq_lens, scale, lse_base, o_part, o_part_dtype, lse_part, workspace, status,
+                       stream);
+}
+
 // ---------------------------------------------------------------------------- allocation-free variant
 // Some callers cannot hand the library a workspace: a serving process that has
 // given every free byte of HBM to its KV pool and forbids further device
@@ -1348,15 +1390,14 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB per device
 __device__ __align__(256) unsigned char g_partial_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_partial_scratch on the current device (looked up once per
 // device; in host code the array's name is only a host-side stand-in).
 void* scratch_address() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
@@ -1377,12 +1418,15 @@ extern "C" int32_t dcp_mla_decode_partial_static(const dcp_layout_t* layout, int
                                                  const int64_t* seq_lens, float scale, int32_t lse_base,
                                                  void* o_part, int32_t o_part_dtype, float* lse_part,
                                                  int32_t* status, void* stream) {
-  const size_t need = dcp_mla_decode_workspace_size(layout, shard_begin, shard_end, B, q_len, H);
-  if (need == 0) return DCP_ERR_INVALID;
-  if (need > kStaticScratchBytes) return DCP_ERR_TOO_LARGE;
+  const int32_t rc = check_decode_args(layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages,
+                                       block_table, bt_stride, max_pages, seq_lens, scale, lse_base, o_part,
+                                       o_part_dtype, lse_part);
+  if (rc != DCP_OK) return rc;
+  Plan p;
+  if (!make_plan(layout, shard_end - shard_begin, B, q_len, H, &p)) return DCP_ERR_CUDA;
+  if (p.ws_total > kStaticScratchBytes) return DCP_ERR_TOO_LARGE;
   void* ws = scratch_address();
   if (!ws) return DCP_ERR_CUDA;
-  return dcp_mla_decode_partial(layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages, block_table,
-                                bt_stride, max_pages, seq_lens, scale, lse_base, o_part, o_part_dtype, lse_part, ws,
-                                kStaticScratchBytes, status, stream);
+  return launch_decode(p, layout, shard_begin, shard_end, q, B, q_len, H, arena, pool_pages, block_table, bt_stride,
+                       max_pages, seq_lens, scale, lse_base, o_part, o_part_dtype, lse_part, ws, status, stream);
 }

@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dcp.h"
 
 namespace dcp {
@@ -62,19 +64,51 @@ inline int32_t launch_status(int64_t launches = 1) {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if unavailable).
+// cuTensorMapEncodeTiled from the driver, looked up once per process (nullptr if
+// unavailable).  The function-local static is initialised under the C++ runtime's
+// own lock, so concurrent first calls from several host threads are safe.
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
   return fn;
 }
+
+constexpr int kMaxDevices = 64;
+
+// The current device, or -1 if it cannot be read or is kMaxDevices or above.
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// A kernel's dynamic shared-memory limit, raised on each device the first time
+// a launch there needs more than the default (cudaFuncSetAttribute acts on the
+// current device only).  One instance per kernel; safe to use from several host
+// threads at once, e.g. one thread per GPU.
+class SmemLimit {
+ public:
+  bool ensure(const void* kernel, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lock(m_);
+    if (set_[dev] >= bytes) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+      return false;
+    set_[dev] = bytes;
+    return true;
+  }
+
+ private:
+  std::mutex m_;
+  size_t set_[kMaxDevices] = {};
+};
 
 }  // namespace dcp

@@ -5,8 +5,9 @@ workspace (a serving process whose HBM is all given to its KV pool, or a plain
 C host with no device-memory manager): it runs on a scratch array the library
 owns.  These tests check that it gives the same partials as
 dcp_mla_decode_partial with a caller workspace, on two calls in a row (the
-second reuses whatever the first left in the shared scratch), and that sizes
-beyond the array are rejected.  This file is collected last on purpose.
+second reuses whatever the first left in the shared scratch), that both match
+the fp64 oracle, and that sizes beyond the array are rejected.  This file is
+collected last on purpose.
 """
 
 import ctypes
@@ -37,6 +38,13 @@ def test_static_scratch_matches_workspace_call(name, over):
     st.decode()                                     # reference: caller-provided workspace
     ref_o = to_f64(st.dec.o_part)
     ref_l = to_f64(st.dec.lse_part)
+    # the oracle's per-shard partials of every request (fp64, from the same input rows)
+    orc_o = np.zeros(ref_o.shape)
+    orc_l = np.zeros(ref_l.shape)
+    for b in range(cfg.B):
+        _o, _l, o_parts, lse_parts = st.oracle_request(b)
+        orc_o[:, b] = o_parts
+        orc_l[:, b] = lse_parts
     for call in range(2):                           # two calls in a row share the scratch
         o_part = torch.full_like(st.dec.o_part, float("nan"))
         lse_part = torch.full_like(st.dec.lse_part, float("nan"))
@@ -44,8 +52,10 @@ def test_static_scratch_matches_workspace_call(name, over):
         _static_call(st, o_part, lse_part, status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert_close_o(to_f64(o_part), ref_o, f"{name} static o_part call {call}")
-        assert_close_lse(to_f64(lse_part), ref_l, f"{name} static lse_part call {call}")
+        assert_close_o(to_f64(o_part), ref_o, f"{name} static o_part call {call} vs workspace call")
+        assert_close_lse(to_f64(lse_part), ref_l, f"{name} static lse_part call {call} vs workspace call")
+        assert_close_o(to_f64(o_part), orc_o, f"{name} static o_part call {call} vs oracle")
+        assert_close_lse(to_f64(lse_part), orc_l, f"{name} static lse_part call {call} vs oracle")
 
 
 def test_static_scratch_rejects_oversized_request():
