@@ -99,8 +99,10 @@ def workload_accounting(cfg, S_b):
     for s in S:
         for t in range(cfg.q_len):
             flops += (s - cfg.q_len + t + 1) * cfg.H * FLOP_PER_TOKEN_ROW
+    # the partial call's own algorithmic bytes: KV and Q read once, each partial
+    # summary written once at the pages' minimum (bf16 o_r + fp32 lse_r)
     return {"kv_bytes": kv_bytes, "bytes_alg": kv_bytes + q_bytes + part_bytes + out_bytes + append_bytes,
-            "flops_alg": flops, "partial_bytes_alg": kv_bytes + q_bytes + cfg.N * cfg.B * R * (512 * 4 + 4)}
+            "flops_alg": flops, "partial_bytes_alg": kv_bytes + q_bytes + parts * (512 * 2 + 4)}
 
 
 class ClockSampler:
@@ -184,7 +186,7 @@ def build_state(cfg, device):
     out_dtype = torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16
     dec = ShardedMlaDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE,
                             dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E, out_dtype,
-                            torch.float32, max_append=max(cfg.B * new, 1), device=device)
+                            torch.float32, device=device)
     btd = bt.to(device)
     # cache: every request holds S_b - new tokens before the step; the step appends the rest
     new_rows, new_pos, new_req = [], [], []

@@ -64,7 +64,7 @@ _SIGNATURES = {
     "dcp_error_string": (ctypes.c_char_p, [_I32]),
     "dcp_count": (_I64, [_LP, _I32, _I64]),
     "dcp_slot_map": (_I32, [_LP, _P, _P, _I64, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
-    "dcp_kv_append": (_I32, [_LP, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _P]),
+    "dcp_kv_append": (_I32, [_LP, _I32, _I32, _P, _P, _P, _I64, _P, _I32, _I64, _I64, _P, _I64, _P, _P]),
     "dcp_kv_relayout": (_I32, [_LP, _I32, _I32, _P, _I64, _I32, _P, _I64, _I64, _P, _P, _I64, _I32, _P, _I64, _I64,
                                _P, _I64, _P, _P]),
     "dcp_mla_decode_partial": (_I32, [_LP, _I32, _I32, _P, _I32, _I32, _I32, _P, _I64, _P, _I64, _I64,
@@ -165,17 +165,21 @@ def dcp_slot_map(layout, pos, req, block_table, max_pages, pool_pages, owner, ro
         _ptr(owner), _ptr(row), _ptr(slot), _ptr(status), _stream(stream)))
 
 
-def dcp_kv_append(layout, shard_begin, shard_end, kv_new, owner, slot, arena, pool_pages, status, stream=None):
-    """Owner-filtered copy of kv_new [T, 576] bf16 into arena [shards, pool_pages*P, 576]."""
+def dcp_kv_append(layout, shard_begin, shard_end, kv_new, pos, req, block_table, max_pages, arena, pool_pages,
+                  status, stream=None):
+    """Owner-filtered write of kv_new [T, 576] bf16 (positions pos, requests req) into
+    arena [shards, pool_pages*P, 576]; placement computed in the same kernel."""
     T = kv_new.shape[0]
     _dev(kv_new, "kv_new", torch.bfloat16, (T, 576))
-    _dev(owner, "owner", torch.int32, (T,))
-    _dev(slot, "slot", torch.int64, (T,))
+    _dev(pos, "pos", torch.int64, (T,))
+    _dev(req, "req", torch.int32, (T,))
+    _dev(block_table, "block_table", torch.int32)
     _dev(arena, "arena", torch.bfloat16, (shard_end - shard_begin, pool_pages * layout.page_size, 576))
     _dev(status, "status", torch.int32, (1,))
+    B, stride = block_table.shape
     _check("dcp_kv_append", load_library().dcp_kv_append(
-        ctypes.byref(layout), shard_begin, shard_end, _ptr(kv_new), _ptr(owner), _ptr(slot), T,
-        _ptr(arena), pool_pages, _ptr(status), _stream(stream)))
+        ctypes.byref(layout), shard_begin, shard_end, _ptr(kv_new), _ptr(pos), _ptr(req), T, _ptr(block_table),
+        B, stride, max_pages, _ptr(arena), pool_pages, _ptr(status), _stream(stream)))
 
 
 def dcp_kv_relayout(layout, shard_begin, shard_end, src_pool, src_page_size, src_block_table, src_max_pages,

@@ -2,10 +2,11 @@
 // relayout (integer / copy kernels).
 //
 // dcp_slot_map: one thread per new token computes (owner, local row, slot).
-// dcp_kv_append: one warp per new token copies its 1152-byte latent row with
-// 16-byte vector loads/stores into the owner's pool.  Both are tiny next to
-// the decode partial (B tokens per decode step; 8192 per chunk), so they are
-// written for latency: one launch each, no shared memory.
+// dcp_kv_append: one warp per new token computes the same placement and copies
+// its 1152-byte latent row with 16-byte vector loads/stores into the owner's
+// pool.  Both are tiny next to the decode partial (B tokens per decode step;
+// 8192 per chunk), so they are written for latency: one launch, no shared
+// memory.
 // dcp_kv_relayout: one warp per listed token of a paged prefill pool: owner
 // filter, source and destination rows, a 1152-byte copy (HBM-bound for long
 // requests: 2 x 1152 bytes per moved token).
@@ -78,25 +79,53 @@ __global__ void slot_map_kernel(Layout L, const int64_t* __restrict__ pos,
   slot[t] = s;
 }
 
-// One warp per token; a 576-element bf16 row is 72 16-byte vectors.
-__global__ void kv_append_kernel(const uint4* __restrict__ kv_new, const int32_t* __restrict__ owner,
-                                 const int64_t* __restrict__ slot, int64_t T, uint4* __restrict__ arena,
-                                 int32_t shard_begin, int32_t shard_end, int64_t pool_rows,
-                                 int32_t* status) {
+// Owner-filtered append: one warp per new token.  Every lane computes the
+// token's owner, local row and slot (the slot map's formulas), so the copy needs
+// no separate slot-map launch; tokens of shards this call does not hold stop
+// before reading their block-table entry.  The 1152-byte row moves as 72
+// 16-byte vectors.  Positions below 2^31 take 32-bit index math.
+__global__ void kv_append_kernel(Layout L, int32_t shard_begin, int32_t shard_end, const uint4* __restrict__ kv_new,
+                                 const int64_t* __restrict__ pos, const int32_t* __restrict__ req, int64_t T,
+                                 const int32_t* __restrict__ bt, int32_t B, int64_t bt_stride, int64_t max_pages,
+                                 uint4* __restrict__ arena, int64_t pool_pages, int32_t* status) {
   constexpr int kVec = kDk * 2 / 16;  // 72
-  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const int32_t own = owner[warp];
+  if (t >= T) return;
+  const int64_t p = __ldg(pos + t);
+  const int32_t b = __ldg(req + t);
+  if (p < 0 || b < 0 || b >= B) {
+    if (lane == 0) flag(status, p < 0 ? DCP_STATUS_BAD_POSITION : DCP_STATUS_BAD_REQUEST);
+    return;
+  }
+  int64_t own, row;
+  if (p < INT32_MAX) {
+    const int32_t p32 = (int32_t)p, blk = p32 / L.I;
+    own = blk % L.N;
+    row = (int64_t)(blk / L.N) * L.I + p32 % L.I;
+  } else {
+    own = owner_of(p, L);
+    row = local_row_of(p, L);
+  }
   if (own < shard_begin || own >= shard_end) return;  // another device's shard
-  const int64_t s = slot[warp];
-  if (s < 0 || s >= pool_rows) {
+  const int64_t pidx = row / L.P;
+  if (pidx >= max_pages) {
+    if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_INDEX);
+    return;
+  }
+  const int64_t page = __ldg(bt + (int64_t)b * bt_stride + pidx);
+  if (page < 0 || page >= pool_pages) {
     if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_ID);
     return;
   }
-  const uint4* src = kv_new + warp * kVec;
-  uint4* dst = arena + ((int64_t)(own - shard_begin) * pool_rows + s) * kVec;
-  for (int i = lane; i < kVec; i += 32) dst[i] = __ldg(src + i);
+  const int64_t slot = page * L.P + row % L.P;
+  const uint4* src = kv_new + t * kVec;
+  uint4* dst = arena + ((own - shard_begin) * pool_pages * L.P + slot) * kVec;
+  uint4 v0 = __ldg(src + lane), v1 = __ldg(src + 32 + lane), v2;
+  if (lane < kVec - 64) v2 = __ldg(src + 64 + lane);
+  dst[lane] = v0;
+  dst[32 + lane] = v1;
+  if (lane < kVec - 64) dst[64 + lane] = v2;
 }
 
 // Prefill-to-decode relayout: one warp per listed token.  The owner filter
@@ -198,21 +227,21 @@ extern "C" int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, 
 }
 
 extern "C" int32_t dcp_kv_append(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
-                                 const void* kv_new, const int32_t* owner, const int64_t* slot,
-                                 int64_t T, void* arena, int64_t pool_pages, int32_t* status,
-                                 void* stream) {
-  if (!layout_ok(layout) || T < 0 || pool_pages < 1 || shard_begin < 0 ||
-      shard_end > layout->n_shards || shard_begin >= shard_end)
+                                 const void* kv_new, const int64_t* pos, const int32_t* req, int64_t T,
+                                 const int32_t* block_table, int32_t B, int64_t bt_stride, int64_t max_pages,
+                                 void* arena, int64_t pool_pages, int32_t* status, void* stream) {
+  if (!layout_ok(layout) || shard_begin < 0 || shard_end > layout->n_shards || shard_begin >= shard_end || T < 0 ||
+      B < 1 || max_pages < 1 || bt_stride < max_pages || pool_pages < 1)
     return DCP_ERR_INVALID;
   if (T == 0) return DCP_OK;
-  if (!kv_new || !owner || !slot || !arena) return DCP_ERR_INVALID;
+  if (!kv_new || !pos || !req || !block_table || !arena) return DCP_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(kv_new) | reinterpret_cast<uintptr_t>(arena)) & 15)
     return DCP_ERR_INVALID;  // rows are moved as 16-byte vectors
   const int threads = 256;  // 8 tokens per block
   const int64_t blocks = (T * 32 + threads - 1) / threads;
   if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
   kv_append_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(
-      static_cast<const uint4*>(kv_new), owner, slot, T, static_cast<uint4*>(arena), shard_begin,
-      shard_end, pool_pages * layout->page_size, status);
+      to_layout(layout), shard_begin, shard_end, static_cast<const uint4*>(kv_new), pos, req, T, block_table, B,
+      bt_stride, max_pages, static_cast<uint4*>(arena), pool_pages, status);
   return launch_status();
 }

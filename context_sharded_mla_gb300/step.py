@@ -1,4 +1,4 @@
-"""A decode step over the C ABI: slot map -> owner-filtered append -> partials -> merge.
+"""A decode step over the C ABI: owner-filtered append -> partials -> merge.
 
 ``ShardedMlaDecoder`` owns the device buffers of one sharded MLA layer held on
 this GPU (the pools of shards [shard_begin, shard_end), the partial outputs,
@@ -12,14 +12,14 @@ from __future__ import annotations
 import torch
 
 from . import (DCP_LSE_BASE_2, DCP_LSE_BASE_E, Layout, dcp_kv_append, dcp_lse_merge,
-               dcp_mla_decode_partial, dcp_mla_decode_workspace_size, dcp_slot_map)
+               dcp_mla_decode_partial, dcp_mla_decode_workspace_size)
 
 
 class ShardedMlaDecoder:
     def __init__(self, layout: Layout, B: int, q_len: int, H: int, pool_pages: int, max_pages: int,
                  scale: float, lse_base: int = DCP_LSE_BASE_E, out_dtype=torch.bfloat16,
                  part_dtype=torch.float32, shard_begin: int = 0, shard_end: int | None = None,
-                 max_append: int = 0, device="cuda"):
+                 device="cuda"):
         self.layout = layout
         self.shard_begin = shard_begin
         self.shard_end = layout.n_shards if shard_end is None else shard_end
@@ -37,25 +37,14 @@ class ShardedMlaDecoder:
         ws = dcp_mla_decode_workspace_size(layout, self.shard_begin, self.shard_end, B, q_len, H)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self._slot_bufs(max(max_append, 1), dev)
-
-    def _slot_bufs(self, T, dev):
-        self.owner = torch.empty(T, dtype=torch.int32, device=dev)
-        self.row = torch.empty(T, dtype=torch.int64, device=dev)
-        self.slot = torch.empty(T, dtype=torch.int64, device=dev)
 
     def append(self, kv_new, pos, req, block_table, stream=None):
-        """Place T new latent rows (kv_new [T, 576] bf16 at positions pos of requests req)."""
-        T = kv_new.shape[0]
-        if T == 0:
+        """Place T new latent rows (kv_new [T, 576] bf16 at positions pos of requests req):
+        one owner-filtered append, placement computed in the kernel."""
+        if kv_new.shape[0] == 0:
             return
-        if self.owner.numel() < T:
-            self._slot_bufs(T, kv_new.device)
-        owner, row, slot = self.owner[:T], self.row[:T], self.slot[:T]
-        dcp_slot_map(self.layout, pos, req, block_table, self.max_pages, self.pool_pages,
-                     owner, row, slot, self.status, stream)
-        dcp_kv_append(self.layout, self.shard_begin, self.shard_end, kv_new, owner, slot,
-                      self.arena, self.pool_pages, self.status, stream)
+        dcp_kv_append(self.layout, self.shard_begin, self.shard_end, kv_new, pos, req, block_table,
+                      self.max_pages, self.arena, self.pool_pages, self.status, stream)
 
     def partial(self, q, block_table, seq_lens, stream=None):
         dcp_mla_decode_partial(self.layout, self.shard_begin, self.shard_end, q, self.arena,

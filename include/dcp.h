@@ -123,13 +123,18 @@ int64_t dcp_count(const dcp_layout_t* layout, int32_t shard, int64_t x);
  *   block_table  int32[B, bt_stride]; entry [b][k] is the physical page (same
  *                id on every shard) holding local rows [k*P, (k+1)*P) of b;
  *                only columns k < max_pages are read
+ *   B            rows of block_table: a token whose request lies outside [0, B)
+ *                is flagged (BAD_REQUEST) instead of read past the table
+ *   pool_pages   pages per shard pool: a page id outside [0, pool_pages) gives
+ *                slot -1 and BAD_PAGE_ID, so no caller writes past a pool
  *   owner  (out) int32[T]  owning shard
  *   row    (out) int64[T]  local row on the owner
  *   slot   (out) int64[T]  row index inside the owner's pool = page * P + row % P,
  *                          or -1 if the token could not be placed (status set)
  *   status (in/out) int32 device word, see DCP_STATUS_*
  * T == 0 is a no-op.  Errors: DCP_ERR_INVALID for a bad layout, T < 0,
- * B < 1, max_pages < 1 or max_pages > bt_stride, or a null pointer with T > 0.
+ * B < 1, max_pages < 1 or max_pages > bt_stride, pool_pages < 1, or a null
+ * pointer with T > 0.
  */
 int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32_t* req,
                      int64_t T, const int32_t* block_table, int32_t B, int64_t bt_stride,
@@ -143,19 +148,30 @@ int32_t dcp_slot_map(const dcp_layout_t* layout, const int64_t* pos, const int32
  * computes the new latent [c_K || k_R]; only the owner stores its row) and
  * section 6 (set_mla_kv_buffer_dcp_sharded); "Decode Context Parallelism"
  * (zdszero), SGLang K3 decode path (the new token's latent is written only to
- * its owner rank).
+ * its owner rank).  Placement is dcp_slot_map's, computed in the same kernel.
  *
- *   kv_new  bf16[T, 576]  new latent rows
- *   owner   int32[T], slot int64[T]: the output of dcp_slot_map
- *   arena   bf16[shard_end - shard_begin, pool_pages * P, 576]: the pools of
- *           shards [shard_begin, shard_end), one after another
- * Token t is copied to arena[owner[t] - shard_begin][slot[t]] when
- * shard_begin <= owner[t] < shard_end; tokens of other shards are skipped
- * (another device holds them); slot < 0 or >= pool_pages * P is skipped and
- * flagged DCP_STATUS_BAD_PAGE_ID.  Rows are copied bit for bit.
+ *   kv_new       bf16[T, 576]  new latent rows
+ *   pos, req     int64[T], int32[T]: request-global position and request index
+ *                of each new token (as for dcp_slot_map)
+ *   block_table  int32[B, bt_stride], columns k < max_pages read (as for
+ *                dcp_slot_map)
+ *   arena        bf16[shard_end - shard_begin, pool_pages * P, 576]: the pools
+ *                of shards [shard_begin, shard_end), one after another
+ * Token t with owner o = (pos / I) % N in [shard_begin, shard_end) is copied bit
+ * for bit to arena[o - shard_begin][slot], slot = block_table[req][row / P] * P
+ * + row % P with row = (pos / (N*I)) * I + pos % I; tokens of other shards are
+ * skipped (another device holds them) and their block-table entries are not
+ * read.  Device status: a negative position (BAD_POSITION) or a request outside
+ * [0, B) (BAD_REQUEST) is flagged for any token; a local row past max_pages
+ * (BAD_PAGE_INDEX) or a page id outside [0, pool_pages) (BAD_PAGE_ID) for a
+ * held token; each skips only that token.  T == 0 is a no-op.  Errors:
+ * DCP_ERR_INVALID for a bad layout or shard range, T < 0, B < 1, max_pages
+ * outside [1, bt_stride], pool_pages < 1, a null pointer with T > 0, or kv_new
+ * / arena not 16-byte aligned.
  */
 int32_t dcp_kv_append(const dcp_layout_t* layout, int32_t shard_begin, int32_t shard_end,
-                      const void* kv_new, const int32_t* owner, const int64_t* slot, int64_t T,
+                      const void* kv_new, const int64_t* pos, const int32_t* req, int64_t T,
+                      const int32_t* block_table, int32_t B, int64_t bt_stride, int64_t max_pages,
                       void* arena, int64_t pool_pages, int32_t* status, void* stream);
 
 /*
@@ -247,7 +263,9 @@ int32_t dcp_mla_decode_partial(const dcp_layout_t* layout, int32_t shard_begin, 
                                int32_t* status, void* stream);
 
 /* Workspace bytes dcp_mla_decode_partial needs for these sizes on the current
- * device (0 on bad arguments).  It does not depend on the sequence lengths. */
+ * device (0 on bad arguments).  It does not depend on the sequence lengths (so
+ * no maximum length is asked for); it depends on the number of shards held,
+ * shard_end - shard_begin, through the (request, shard) work units. */
 size_t dcp_mla_decode_workspace_size(const dcp_layout_t* layout, int32_t shard_begin,
                                      int32_t shard_end, int32_t B, int32_t q_len, int32_t H);
 

@@ -44,8 +44,7 @@ class GpuState:
         self.seq_lens = self.S.to(dev)
         od = out_dtype or (torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16)
         self.dec = ShardedMlaDecoder(self.layout, cfg.B, cfg.q_len, cfg.H, self.pool_pages, self.max_pages,
-                                     workloads.SCALE, 1 if cfg.base == 2 else 0, od, part_dtype,
-                                     max_append=int(self.S.max()))
+                                     workloads.SCALE, 1 if cfg.base == 2 else 0, od, part_dtype)
         self.needle_pos = workloads.needle_positions(cfg, self.S) if needle else None
         self.kv = {}
         for b in range(cfg.B):

@@ -37,6 +37,54 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def declared_parameters():
+    """{function name: [parameter declarations]} from include/dcp.h."""
+    src = open(os.path.join(ROOT, "include", "dcp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(dcp_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = params
+    return out
+
+
+# The calls the boundary specification lists, with its argument count, and every
+# argument this library adds, with why (the departures are stated in the design
+# notes as readings).
+BOUNDARY = {
+    "dcp_count": (3, []),
+    "dcp_slot_map": (12, ["B", "pool_pages"]),                   # range checks of req and of page ids
+    "dcp_kv_append": (12, ["shard_begin", "shard_end", "B"]),    # pools held by this device; req range check
+    "dcp_mla_decode_partial": (22, []),
+    "dcp_mla_decode_workspace_size": (5, ["shard_begin", "shard_end", "-max_seq"]),  # units depend on shards held,
+                                                                                     # not on any length
+    "dcp_lse_merge": (10, []),
+}
+
+
+def test_boundary_argument_counts():
+    params = declared_parameters()
+    for name, (spec_count, changes) in BOUNDARY.items():
+        assert name in params, name
+        added = sum(1 for c in changes if not c.startswith("-"))
+        removed = sum(1 for c in changes if c.startswith("-"))
+        assert len(params[name]) == spec_count + added - removed, (name, params[name])
+        names = [p.split()[-1].lstrip("*") for p in params[name]]
+        for c in changes:
+            if c.startswith("-"):
+                assert c[1:] not in names, (name, c)
+            else:
+                assert c in names, (name, c)
+
+
+def test_binding_signatures_match_the_header():
+    import context_sharded_mla_gb300 as dcp
+    params = declared_parameters()
+    for name, (_res, args) in dcp._SIGNATURES.items():
+        assert name in params, f"{name} bound but not declared"
+        assert len(args) == len(params[name]), (name, len(args), params[name])
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in include/dcp.h but not exported"
@@ -69,8 +117,24 @@ def test_host_validation_rejects_bad_arguments(lib):
                             P(16), None) == -1
     assert lib.dcp_slot_map(ctypes.byref(good), P(16), P(16), 0, P(16), 1, 1, 1, 1, P(16), P(16), P(16),
                             P(16), None) == 0       # T == 0 is a no-op
-    assert lib.dcp_kv_append(ctypes.byref(good), 0, 5, P(16), P(16), P(16), 1, P(16), 1, P(16), None) == -1
-    assert lib.dcp_kv_append(ctypes.byref(good), 0, 4, P(17), P(16), P(16), 1, P(16), 1, P(16), None) == -1
+    # append: (layout, shard_begin, shard_end, kv_new, pos, req, T, block_table, B, bt_stride, max_pages,
+    #          arena, pool_pages, status, stream)
+    ap = lambda **kw: dict(dict(sb=0, se=4, kv=P(16), pos=P(16), req=P(16), T=1, bt=P(16), B=1, st=1, mp=1,
+                                ar=P(16), pp=1, status=P(16)), **kw)
+
+    def append(**kw):
+        a = ap(**kw)
+        return lib.dcp_kv_append(ctypes.byref(good), a["sb"], a["se"], a["kv"], a["pos"], a["req"], a["T"], a["bt"],
+                                 a["B"], a["st"], a["mp"], a["ar"], a["pp"], a["status"], None)
+    assert append(T=0) == 0                         # no-op, nothing launched
+    assert append(se=5) == -1
+    assert append(kv=P(17)) == -1                   # not 16-byte aligned
+    assert append(B=0) == -1
+    assert append(mp=2, st=1) == -1
+    assert append(pp=0) == -1
+    assert append(pos=None) == -1
+    assert lib.dcp_kv_append(ctypes.byref(bad), 0, 4, P(16), P(16), P(16), 1, P(16), 1, 1, 1, P(16), 1, P(16),
+                             None) == -1
     # decode: q_len*H over the limit, bad base, bad dtype, missing workspace
     args = lambda **kw: dict(dict(sb=0, se=4, q=P(256), B=1, ql=1, H=16, ar=P(256), pp=1, bt=P(256), st=1, mp=1,
                                   sl=P(256), sc=0.1, base=0, op=P(256), od=0, lp=P(256), ws=None, wsb=0,
@@ -89,6 +153,16 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert call(se=5) == -1
     assert call(q=None) == -1
     assert call(mp=2, st=1) == -1
+    # the allocation-free variant checks its arguments the same way, before any CUDA call
+
+    def call_static(**kw):
+        a = args(**kw)
+        return lib.dcp_mla_decode_partial_static(ctypes.byref(good), a["sb"], a["se"], a["q"], a["B"], a["ql"],
+                                                 a["H"], a["ar"], a["pp"], a["bt"], a["st"], a["mp"], a["sl"],
+                                                 a["sc"], a["base"], a["op"], a["od"], a["lp"], a["status"], None)
+    for bad_arg in (dict(H=65537), dict(base=7), dict(od=9), dict(sc=-1.0), dict(se=5), dict(q=None),
+                    dict(mp=2, st=1), dict(q=P(264))):
+        assert call_static(**bad_arg) == -1, bad_arg
     need = lib.dcp_mla_decode_workspace_size(ctypes.byref(good), 0, 4, 1, 1, 16)
     if need > 0:
         assert call(wsb=need - 1, ws=P(256)) == -4

@@ -100,8 +100,7 @@ def test_running_max_jumps(H, N):
     bt, pool_pages = workloads.block_table(cfg, S)
     dev = "cuda"
     lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
-    dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, 1,
-                            max_append=int(S.max()))
+    dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, 1)
     q = workloads.gen_q(cfg)
     btd = bt.to(dev)
     kvs = []
@@ -199,8 +198,7 @@ def test_decode_step_with_append():
     bt, pool_pages = workloads.block_table(cfg, S)
     dev = "cuda"
     lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
-    dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, 1,
-                            max_append=int(S.max()))
+    dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, 1)
     kvs = [workloads.gen_kv(cfg, b, int(S[b])) for b in range(cfg.B)]
     btd = bt.to(dev)
     for b in range(cfg.B):

@@ -29,7 +29,7 @@ def test_decode_step_replays_in_a_cuda_graph():
     bt, pool_pages = workloads.block_table(cfg, S)
     lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
     dec = ShardedMlaDecoder(lay, cfg.B, 1, cfg.H, pool_pages, bt.shape[1], workloads.SCALE,
-                            dcp.DCP_LSE_BASE_2, torch.float32, max_append=int(S.max()), device=dev)
+                            dcp.DCP_LSE_BASE_2, torch.float32, device=dev)
     btd = bt.to(dev)
     kv = [workloads.gen_kv(cfg, b, int(S[b])) for b in range(cfg.B)]
     first = int(S[0]) - 3                     # the cache holds S - 3 tokens; three steps append the rest
