@@ -14,6 +14,7 @@ The oracle is written from these pages (quoted by title and section):
   count(a+L) - count(a); idea 2: each shard hands over (O_r, L_r)), section
   "Theory" (derivation of the merge identity, the merge operator and its
   numerically stable form, the base-e / base-2 pairing rule);
+  section "通信策略" (the all-to-all and the AllGather + ReduceScatter merges);
   section "decode 路径：以 Kimi K3 的 MLA 为例" (w_kc / w_vc shapes).
 * "MLA 的 Decode Context Parallelism" (ggaaooppeenngg.github.io): section 2
   (absorbed form: 576-d single-KV-head MQA, V = the 512-d c_K part, and the
@@ -35,9 +36,11 @@ Modules
 ``attention``   per-shard partial (o_r, lse_r), LSE merge, unsharded attention.
 ``bruteforce``  pure-Python loop versions for tiny inputs (pins for the above).
 ``absorb``      the query-side and output-side absorption products (identities 1, 2).
+``exchange``    the cross-rank exchange of the partials: the all-to-all by head slice
+                (and its wire format) and the AllGather + ReduceScatter merge.
 
 Every function here is pinned by a ``-m "not gpu"`` test against the pages'
 worked examples, closed forms, invariants or brute force.  None is unpinned.
 """
 
-from . import layout, attention, bruteforce, absorb  # noqa: F401
+from . import layout, attention, bruteforce, absorb, exchange  # noqa: F401
