@@ -33,8 +33,9 @@ Readings (the pages assume one shard per rank and H divisible by the group):
 * Wire format of one rank's all-to-all send buffer (the library's format, so the
   byte layout has a definition to compare with): for each destination d in
   order, an o block [n_held, T, H/W, 512] in the wire dtype (bf16 rounded to
-  nearest even, or f32) followed by an lse block [n_held, T, H/W] f32, where T
-  is the number of query tokens (B * q_len) and n_held = N / W.
+  nearest even, or f32) followed by an lse block [n_held, T, H/W] f32, the two
+  padded with zero bytes to a multiple of 256 bytes (so that every chunk starts
+  aligned), where T is the number of query tokens (B * q_len) and n_held = N / W.
 """
 
 from __future__ import annotations
@@ -152,14 +153,17 @@ def pack(o_held, lse_held, W: int, wire_bf16: bool):
         o = o_held[:, :, h0:h1]
         ob = to_bf16_bits(o).tobytes() if wire_bf16 else np.asarray(o, np.float32).tobytes()
         lb = np.ascontiguousarray(lse_held[:, :, h0:h1], dtype=np.float32).tobytes()
-        chunks.append(np.frombuffer(ob + lb, dtype=np.uint8))
+        pad = bytes(-(len(ob) + len(lb)) % 256)
+        chunks.append(np.frombuffer(ob + lb + pad, dtype=np.uint8))
     return np.stack(chunks)
 
 
 def chunk_bytes(n_held: int, T: int, H: int, W: int, wire_bf16: bool) -> int:
-    """Bytes one rank sends to each rank: n_held * T * (H/W) * (512 * e + 4)."""
+    """Bytes one rank sends to each rank: n_held * T * (H/W) * (512 * e + 4),
+    rounded up to a multiple of 256."""
     hd = head_range(0, H, W)[1]
-    return n_held * T * hd * (512 * (2 if wire_bf16 else 4) + 4)
+    n = n_held * T * hd * (512 * (2 if wire_bf16 else 4) + 4)
+    return n + (-n % 256)
 
 
 def unpack(recv, n_held: int, T: int, H: int, W: int, wire_bf16: bool):
@@ -178,7 +182,8 @@ def unpack(recv, n_held: int, T: int, H: int, W: int, wire_bf16: bool):
         else:
             o = np.frombuffer(raw[:ob], dtype=np.float32)
         os_.append(o.astype(np.float64).reshape(n_held, T, hd, 512))
-        ls_.append(np.frombuffer(raw[ob:], dtype=np.float32).astype(np.float64).reshape(n_held, T, hd))
+        ls_.append(np.frombuffer(raw[ob:ob + 4 * n_held * T * hd], dtype=np.float32).astype(np.float64)
+                   .reshape(n_held, T, hd))
     return np.concatenate(os_), np.concatenate(ls_)
 
 

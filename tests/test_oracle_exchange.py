@@ -84,6 +84,10 @@ def test_wire_bytes_match_the_page_accounting():
     rng = np.random.default_rng(3)
     buf = exchange.pack(rng.standard_normal((1, 64, 96, 512)), rng.standard_normal((1, 64, 96)), 8, True)
     assert buf.shape == (8, per_dest)
+    # a chunk that is not a multiple of 256 bytes is padded with zeros
+    assert exchange.chunk_bytes(2, 5, 8, 4, True) == 20736 > 2 * 5 * 2 * (1024 + 4)
+    buf = exchange.pack(rng.standard_normal((2, 5, 8, 512)), rng.standard_normal((2, 5, 8)), 4, True)
+    assert buf.shape == (4, 20736) and not buf[:, 2 * 5 * 2 * 1028:].any()
 
 
 @pytest.mark.parametrize("wire_bf16", [False, True])
