@@ -87,45 +87,60 @@ def a2a_merge(o_parts, lse_parts, W: int, base=0):
     return [merge(o_d, l_d, base) for o_d, l_d in a2a_received(o_parts, lse_parts, W)]
 
 
+def global_lse(lse_all, base=0):
+    """Step 1 of AllGather + ReduceScatter: from the gathered lse of all N shards
+    [N, ...], L = m + log sum_r exp(lse_r - m) (log2 / exp2 in base 2); rows
+    whose shards are all empty get -inf."""
+    base = 2 if base in (1, 2) else 0
+    lse_all = np.asarray(lse_all, dtype=np.float64)
+    m = lse_all.max(axis=0)
+    empty = np.isneginf(m)
+    m_safe = np.where(empty, 0.0, m)
+    pw = np.exp2 if base == 2 else np.exp
+    Z = np.where(empty, 1.0, pw(lse_all - m_safe).sum(axis=0))
+    return np.where(empty, -np.inf, m_safe + (np.log2(Z) if base == 2 else np.log(Z)))
+
+
+def rescale_local(lse_all, o_held, shard_begin: int, W: int, base=0):
+    """Step 2 on one rank: sum over its held shards s of exp(lse_s - L) * O_s
+    (2 ** (lse_s - L) in base 2; an empty shard contributes 0), with L from
+    global_lse.  lse_all [N, T, H] (every shard), o_held [n_held, T, H, 512].
+    Returned head-sliced for the reduce-scatter: (o_sum [W, T, H/W, 512],
+    L [W, T, H/W]); block d holds heads [d*H/W, (d+1)*H/W)."""
+    base = 2 if base in (1, 2) else 0
+    lse_all = np.asarray(lse_all, dtype=np.float64)
+    o_held = np.asarray(o_held, dtype=np.float64)
+    n_held = o_held.shape[0]
+    L = global_lse(lse_all, base)
+    L_safe = np.where(np.isneginf(L), 0.0, L)
+    pw = np.exp2 if base == 2 else np.exp
+    wgt = pw(lse_all[shard_begin:shard_begin + n_held] - L_safe)   # exp(-inf) = 0 for an empty shard
+    total = (wgt[..., None] * o_held).sum(axis=0)
+    total = np.where(np.isneginf(L)[..., None], 0.0, total)
+    H = lse_all.shape[2]
+    blocks = [head_range(d, H, W) for d in range(W)]
+    return (np.stack([total[:, h0:h1] for h0, h1 in blocks]), np.stack([L[:, h0:h1] for h0, h1 in blocks]))
+
+
 def ag_rs_merge(o_parts, lse_parts, W: int, base=0):
     """The AllGather + ReduceScatter strategy end to end.
 
-    1. all-gather: every rank sees lse_r of all N shards and forms the global
-       L = m + log sum_r exp(lse_r - m) (log2 / exp2 in base 2; all shards
-       empty -> L = -inf);
-    2. each rank w corrects its own shards: sum over its r of exp(lse_r - L) * O_r
-       (2 ** (lse_r - L) in base 2; an empty shard contributes 0);
+    1. all-gather: every rank sees lse_r of all N shards and forms the global L
+       (global_lse);
+    2. each rank w corrects its own shards (rescale_local);
     3. reduce-scatter: the ranks' corrected sums are added and rank d keeps heads
        [d*H/W, (d+1)*H/W).
     Returns a list over d of (o [T, H/W, 512], lse [T, H/W]).
     """
-    base = 2 if base in (1, 2) else 0
     o_parts = np.asarray(o_parts, dtype=np.float64)
     lse_parts = np.asarray(lse_parts, dtype=np.float64)
-    N, _T, H = lse_parts.shape
-    # step 1: the global L from the gathered lse
-    m = lse_parts.max(axis=0)
-    empty = np.isneginf(m)
-    m_safe = np.where(empty, 0.0, m)
-    pw = (lambda x: np.exp2(x)) if base == 2 else (lambda x: np.exp(x))
-    Z = pw(lse_parts - m_safe).sum(axis=0)
-    L = np.where(empty, -np.inf, m_safe + (np.log2(np.where(empty, 1.0, Z)) if base == 2
-                                           else np.log(np.where(empty, 1.0, Z))))
-    L_safe = np.where(empty, 0.0, L)
-    # step 2: each rank's corrected local sum over its own shards (all heads)
-    corrected = []
+    N = lse_parts.shape[0]
+    sums, L = None, None
     for w in range(W):
         s0, s1 = shard_range(w, N, W)
-        wgt = pw(lse_parts[s0:s1] - L_safe)                # exp(-inf) = 0 for an empty shard
-        corrected.append((wgt[..., None] * o_parts[s0:s1]).sum(axis=0))
-    # step 3: sum over ranks, scattered by head
-    total = np.sum(corrected, axis=0)
-    total = np.where(empty[..., None], 0.0, total)
-    out = []
-    for d in range(W):
-        h0, h1 = head_range(d, H, W)
-        out.append((total[:, h0:h1], L[:, h0:h1]))
-    return out
+        o_sum, L = rescale_local(lse_parts, o_parts[s0:s1], s0, W, base)
+        sums = o_sum if sums is None else sums + o_sum
+    return [(sums[d], L[d]) for d in range(W)]
 
 
 def to_bf16_bits(x):
