@@ -527,14 +527,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       };
-      // lane l: pool rows of the boxes of tile tile0 + l from their page ids (-1: no box)
-      auto to_rows = [&](int rs, int32_t tile0, const int32_t (&pg)[8], int32_t (&yb)[8]) {
-        const int32_t rho0 = (tile0 + lane) * kTile;
+      // lane l: pool rows of the boxes of tile tile0 + l from their page ids (-1: no box).
+      // Which boxes are needed is recomputed here, not read from the -2 marks, so a
+      // block-table entry of -2 is reported like any other bad page id.
+      auto to_rows = [&](int rs, int32_t tile0, int32_t tile_end, int64_t nvis, const int32_t (&pg)[8],
+                         int32_t (&yb)[8]) {
+        const int32_t tile = tile0 + lane;
+        const int32_t rho0 = tile * kTile;
         const int32_t pool0 = rs * (int32_t)a.pool_rows;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           yb[q] = -1;
-          if (pg[q] == -2) continue;
+          if (!(tile < tile_end && q < nbox && rho0 + q * a.box_rows < nvis)) continue;
           if (pg[q] < 0 || pg[q] >= a.pool_pages) {
             if (rank == 0) flag(a.status, DCP_STATUS_BAD_PAGE_ID);
             continue;
@@ -619,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // current 32 are issued; each lane turns its tile's entries into TMA rows
         int32_t pgn[8], yc[8], yn = -1;  // yn: next batch's first-box rows (L2 prefetch)
         fetch_batch(b, nvis, t0, t_end, pgn);
-        to_rows(rs, t0, pgn, yc);
+        to_rows(rs, t0, t_end, nvis, pgn, yc);
         fetch_batch(b, nvis, t0 + 32, t_end, pgn);
         // the query's chunk 4r + 3 and its rope dims [32r, 32r + 32) for the SS part of QK
         if (!warp_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s, lane)) { ok = false; break; }
@@ -634,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++seg;
         for (int jj = 0; jj < nt && ok; ++jj) {
           if (jj > 0 && (jj & 31) == 0) {
-            to_rows(rs, t0 + jj, pgn, yc);
+            to_rows(rs, t0 + jj, t_end, nvis, pgn, yc);
             fetch_batch(b, nvis, t0 + jj + 32, t_end, pgn);
           }
           if (nbox == 1) {
