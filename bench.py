@@ -6,14 +6,20 @@ partials of every shard, and the LSE merge.  The default workload is the
 K3-shaped configuration (B=64, H=96, S=131072, N=8 token round-robin shards,
 page 64, base-2 LSE, one appended token per request per step).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3|dsv3|ragged|long|tiny]
-                  [--op decode|relayout|absorb]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3|dsv3|ragged|long|tiny|extend]
+                  [--op decode|relayout|absorb] [--exchange a2a|ag_rs] [--group]
                   [--impl ours|reference] [--batch B] [--no-cpu-baseline] [--no-e2e]
 
 `value` is KV-read GB/s (sum over requests of S_b * 1152 bytes per step,
-divided by the device time per step; summed over ranks for N > 1, where every
-rank runs its own replica of the workload).  --impl reference times the fp64
-CPU oracle on a bounded sample of the same workload instead.
+divided by the device time per step).  With --gpus N > 1 (under torchrun) the
+same step runs as Decode Context Parallelism over the N GPUs: each rank holds
+N_shards / N of the shards, computes their partials for all heads, and the
+partials are exchanged over NCCL (--exchange a2a: packed all-to-all by head
+slice and a local merge; ag_rs: AllGather of the lse + ReduceScatter) so that
+each rank ends with the merged output of H / N heads; total work is fixed
+(strong scaling) and `value` is the whole job's KV GB/s over the slowest rank's
+step time.  --impl reference times the fp64 CPU oracle on a bounded sample of
+the same workload instead.
 """
 
 from __future__ import annotations
@@ -175,7 +181,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_state(cfg, device):
+def build_state(cfg, device, rank=0, world=1, strategy=None):
+    """The workload's cache appended into this rank's decoder: all N shards on one
+    GPU (world == 1), or, with a DCP group, this rank's N / world shards."""
     import context_sharded_mla_gb300 as dcp
     from context_sharded_mla_gb300.step import ShardedMlaDecoder
     dcp.load_library()
@@ -184,9 +192,14 @@ def build_state(cfg, device):
     lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
     new = max(cfg.append, cfg.chunk)
     out_dtype = torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16
-    dec = ShardedMlaDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE,
-                            dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E, out_dtype,
-                            torch.float32, device=device)
+    base = dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E
+    if strategy is None:
+        dec = ShardedMlaDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, base,
+                                out_dtype, torch.float32, device=device)
+    else:
+        from context_sharded_mla_gb300.group import DcpGroupDecoder
+        dec = DcpGroupDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, rank, world,
+                              base, strategy, torch.bfloat16, out_dtype, torch.float32, device=device)
     btd = bt.to(device)
     # cache: every request holds S_b - new tokens before the step; the step appends the rest
     new_rows, new_pos, new_req = [], [], []
@@ -213,26 +226,52 @@ def build_state(cfg, device):
     return st
 
 
+def held_kv_rows(cfg, S, shard_begin, shard_end):
+    """KV rows of shards [shard_begin, shard_end) over all requests (the library's count)."""
+    import context_sharded_mla_gb300 as dcp
+    lay = dcp.Layout(cfg.N, cfg.I, cfg.P)
+    return sum(dcp.dcp_count(lay, r, int(s)) for s in S for r in range(shard_begin, shard_end))
+
+
 def run_ours(args, cfg, rank, world, dist, device):
     import context_sharded_mla_gb300 as dcp
-    st = build_state(cfg, device)
+    group = world > 1 or args.group
+    if group:
+        # Decode Context Parallelism over the ranks: N / world shards per GPU, heads
+        # split H / world per GPU after the exchange; total work fixed (strong scaling)
+        if cfg.N % world or cfg.H % world:
+            raise SystemExit(f"{cfg.name}: {cfg.N} shards and {cfg.H} heads must split evenly over {world} GPUs")
+    st = build_state(cfg, device, rank, world, args.exchange if group else None)
     dec = st["dec"]
     acct = workload_accounting(cfg, st["S"])
+    if group:
+        sb, se = dec.local.shard_begin, dec.local.shard_end
+        n_held = se - sb
+        R = cfg.q_len * cfg.H
+        # this rank's share of the partial call: its shards' KV, the replicated query, its partial summaries
+        acct["partial_bytes_alg"] = (held_kv_rows(cfg, st["S"], sb, se) * KV_ROW_BYTES + cfg.B * R * 576 * 2
+                                     + n_held * cfg.B * R * (512 * 2 + 4))
+        acct["flops_alg_rank"] = acct["flops_alg"] * n_held / cfg.N
     stream = torch.cuda.current_stream()
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
     ev_part = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
 
+    local = dec.local if group else dec
+
     def step(i=None):
         if st["kv_new"] is not None:
             dec.append(st["kv_new"], st["pos"], st["req"], st["bt"])
         if i is not None:
             ev_part[i][0].record(stream)
-        dec.partial(st["q"], st["bt"], st["seq_lens"])
+        local.partial(st["q"], st["bt"], st["seq_lens"])
         if i is not None:
             ev_part[i][1].record(stream)
-        dec.merge()
+        if group:
+            dec.xchg.exchange(local.o_part, local.lse_part)
+        else:
+            dec.merge()
 
     for _ in range(args.warmup):
         step()
@@ -263,7 +302,7 @@ def run_ours(args, cfg, rank, world, dist, device):
     if dec.status_bits() != 0:
         raise RuntimeError(f"device status {dec.status_bits()} after the timed steps")
     ms_per_step = max_over_ranks(dist, total_ms / args.steps)
-    part_ms_avg = sum(part_ms) / len(part_ms)
+    part_ms_avg = max_over_ranks(dist, sum(part_ms) / len(part_ms))
 
     # end-to-end through the public API with host buffers (H2D inputs, D2H result each step)
     e2e = None
@@ -271,12 +310,13 @@ def run_ours(args, cfg, rank, world, dist, device):
         e2e = run_e2e(args, cfg, st, dist, acct)
 
     peaks = load_peaks()
+    # the whole job's KV per step (all shards on all ranks) over the step time
     kv_gbs = acct["kv_bytes"] / (ms_per_step * 1e-3) / 1e9
-    t_hbm = acct["bytes_alg"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = acct["flops_alg"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = acct["bytes_alg"] / (peaks["hbm_gbs"] * 1e9 * world)
+    t_tc = acct["flops_alg"] / (peaks["bf16_tflops"] * 1e12 * world)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     partial_achieved = acct["partial_bytes_alg"] / (part_ms_avg * 1e-3) / 1e9
-    part_flops = acct["flops_alg"] / (part_ms_avg * 1e-3) / 1e12
+    part_flops = acct.get("flops_alg_rank", acct["flops_alg"]) / (part_ms_avg * 1e-3) / 1e12
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(partial_achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(partial_achieved / peaks["hbm_gbs"], 4)}
@@ -286,9 +326,13 @@ def run_ours(args, cfg, rank, world, dist, device):
     roof["traffic"] = recorded_traffic(cfg.name) if args.batch is None else None
     roof["kernel"] = "dcp_mla_decode_partial (all its launches, CUDA events on the launching stream)"
     roof["peak_source"] = f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured" else "fallback"
+    if group:
+        roof["kernel"] = ("dcp_mla_decode_partial of this rank's shards (all its launches, CUDA events on the "
+                          "launching stream; max over ranks)")
+        roof["traffic"] = None
     result = {
         "metric": METRIC,
-        "value": round(kv_gbs * world, 2),
+        "value": round(kv_gbs, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -298,7 +342,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         "roofline_frac_step": round(max(t_hbm, t_tc) / (ms_per_step * 1e-3), 4),
         "step_binding_roofline": bound,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if group else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 latent rows and queries, shuffled block table)",
@@ -310,6 +354,11 @@ def run_ours(args, cfg, rank, world, dist, device):
         "e2e": e2e,
         "clocks": clk,
     }
+    if group:
+        result["exchange"] = {"strategy": args.exchange, "collectives": "NCCL (torch.distributed)",
+                              "bytes_per_rank_per_step": dec.xchg.bytes_sent(),
+                              "shards_per_gpu": dec.local.shard_end - dec.local.shard_begin,
+                              "heads_per_gpu": dec.head_end - dec.head_begin}
     return result
 
 
@@ -611,8 +660,10 @@ def run_e2e(args, cfg, st, dist, acct):
         kv_host = st["kv_new"].cpu().pin_memory()
         pos_host = st["pos"].cpu().pin_memory()
         req_host = st["req"].cpu().pin_memory()
-    o_host = torch.empty(dec.o.shape, dtype=dec.o.dtype).pin_memory()
-    lse_host = torch.empty(dec.lse.shape, dtype=torch.float32).pin_memory()
+    group = hasattr(dec, "xchg")            # a DCP group rank: its output is its heads' slice
+    o_out, lse_out = (dec.xchg.o, dec.xchg.lse) if group else (dec.o, dec.lse)
+    o_host = torch.empty(o_out.shape, dtype=o_out.dtype).pin_memory()
+    lse_host = torch.empty(lse_out.shape, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(st["q"])
     seq_dev = torch.empty_like(st["seq_lens"])
     if has_new:
@@ -634,8 +685,8 @@ def run_e2e(args, cfg, st, dist, acct):
             o, lse = dec.step(q_dev, st["bt"], seq_dev, kv_dev, pos_dev, req_dev)
         else:
             o, lse = dec.step(q_dev, st["bt"], seq_dev)
-        o_host.copy_(o, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
+        o_host.copy_(o.reshape(o_host.shape), non_blocking=True)
+        lse_host.copy_(lse.reshape(lse_host.shape), non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -649,10 +700,12 @@ def run_e2e(args, cfg, st, dist, acct):
     t1.record(stream)
     barrier(dist)
     ms = max_over_ranks(dist, t0.elapsed_time(t1) / n)
-    world = dist.get_world_size() if dist is not None else 1
-    return {"value": round(acct["kv_bytes"] / (ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+    path = ("DcpGroupDecoder.step over the C ABI and NCCL (query replicated to every rank, each rank reads back "
+            "its heads' o / lse), pinned host buffers" if group else
+            "ShardedMlaDecoder.step over the C ABI, pinned host buffers")
+    return {"value": round(acct["kv_bytes"] / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "path": "ShardedMlaDecoder.step over the C ABI, pinned host buffers"}
+            "steps": n, "path": path}
 
 
 def recorded_traffic(key):
@@ -684,7 +737,9 @@ def config_dict(cfg, st, world):
          "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P, "lse_base": "2" if cfg.base == 2 else "e",
          "new_tokens_per_request": max(cfg.append, cfg.chunk), "out_dtype": cfg.out_dtype,
          "partials": "fp32", "global_batch": cfg.B, "seq_len": int(S.max()),
-         "parallelism": "1 GPU holds all N shards" if world == 1 else f"{world} independent replicas",
+         "parallelism": ("1 GPU holds all N shards" if not hasattr(st["dec"], "xchg") else
+                         f"DCP over {world} GPUs: {cfg.N // world} shards and {cfg.H // world} output heads per GPU, "
+                         f"query replicated, {getattr(st['dec'].xchg, 'strategy', '')} exchange of the partials"),
          "l2": f"inputs larger than L2 ({int(S.sum()) * KV_ROW_BYTES / 1e9:.2f} GB of KV per step), no flush"}
     return d
 
@@ -820,6 +875,12 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--group", action="store_true",
+                    help="run the multi-GPU (DCP group) step even with --gpus 1: the exchange kernels run, the "
+                         "collectives are skipped")
+    ap.add_argument("--exchange", default="a2a", choices=["a2a", "ag_rs"],
+                    help="with --gpus N > 1: all-to-all of the packed partials (default) or AllGather(lse) + "
+                         "ReduceScatter")
     ap.add_argument("--op", default="decode", choices=["decode", "relayout", "absorb"],
                     help="decode: the decode step (default); relayout: the prefill-to-decode relayout; "
                          "absorb: the two absorption products")
@@ -844,6 +905,7 @@ def main(argv=None):
         raise SystemExit("bench.py --impl ours needs a CUDA GPU")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")   # plain NVLink transfers, no multicast objects
     dist = init_dist(world, "nccl")
     if args.op in ("relayout", "absorb"):
         run_op, time_op = ((run_relayout_op, time_oracle_relayout) if args.op == "relayout"

@@ -10,7 +10,8 @@ works but the first call raises ``RuntimeError``.
 Functions (same names as the C ABI):
   dcp_count, dcp_slot_map, dcp_kv_append, dcp_mla_decode_partial,
   dcp_mla_decode_workspace_size, dcp_lse_merge, dcp_kv_relayout, dcp_absorb_q,
-  dcp_absorb_o
+  dcp_absorb_o, dcp_a2a_chunk_bytes, dcp_pack_partials, dcp_lse_merge_packed,
+  dcp_lse_rescale
 """
 
 from __future__ import annotations
@@ -27,6 +28,7 @@ __all__ = [
     "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
     "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count", "dcp_kv_relayout",
     "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes", "dcp_absorb_q", "dcp_absorb_o",
+    "dcp_a2a_chunk_bytes", "dcp_pack_partials", "dcp_lse_merge_packed", "dcp_lse_rescale",
     "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
 ]
 
@@ -76,6 +78,10 @@ _SIGNATURES = {
     "dcp_mla_decode_static_scratch_bytes": (_SZ, []),
     "dcp_absorb_q": (_I32, [_I64, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "dcp_absorb_o": (_I32, [_I64, _I32, _P, _I32, _P, _P, _I32, _P, _P]),
+    "dcp_a2a_chunk_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "dcp_pack_partials": (_I32, [_I32, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P]),
+    "dcp_lse_merge_packed": (_I32, [_I32, _I32, _I64, _P, _I32, _I32, _P, _I32, _P, _P]),
+    "dcp_lse_rescale": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I32, _I32, _P, _P, _P]),
 }
 
 
@@ -337,3 +343,77 @@ def dcp_absorb_o(o, w_vc, v, status=None, stream=None):
     T = o.numel() // (H * 512)
     _check("dcp_absorb_o", load_library().dcp_absorb_o(
         T, H, _ptr(o), _dtype_code(o), _ptr(w_vc), _ptr(v), _dtype_code(v), _ptr(status), _stream(stream)))
+
+
+def dcp_a2a_chunk_bytes(n_held, T, H, world, wire_dtype=torch.bfloat16) -> int:
+    """Bytes of one destination's chunk of an all-to-all buffer (see include/dcp.h)."""
+    code = DCP_BF16 if wire_dtype == torch.bfloat16 else DCP_F32
+    n = int(load_library().dcp_a2a_chunk_bytes(n_held, T, H, world, code))
+    if n == 0:
+        raise DcpError("dcp_a2a_chunk_bytes", DCP_ERR_INVALID, "invalid argument")
+    return n
+
+
+def dcp_pack_partials(o_part, lse_part, world, send, wire_dtype=torch.bfloat16, stream=None):
+    """Pack o_part [n_held, ..., H, 512] / lse_part [n_held, ..., H] by head slice into
+    send (uint8, [world, chunk]) for an all-to-all."""
+    n_held, H = o_part.shape[0], o_part.shape[-2]
+    T = o_part.numel() // (n_held * H * 512) if o_part.numel() else 0
+    _dev(o_part, "o_part", o_part.dtype)
+    if o_part.shape[-1] != 512:
+        raise ValueError("o_part's last dim must be 512")
+    _dev(lse_part, "lse_part", torch.float32)
+    if lse_part.numel() != n_held * T * H:
+        raise ValueError("lse_part must hold n_held * T * H values")
+    chunk = dcp_a2a_chunk_bytes(n_held, T, H, world, wire_dtype)
+    _dev(send, "send", torch.uint8)
+    if send.numel() != world * chunk:
+        raise ValueError(f"send must hold world * chunk = {world * chunk} bytes")
+    code = DCP_BF16 if wire_dtype == torch.bfloat16 else DCP_F32
+    _check("dcp_pack_partials", load_library().dcp_pack_partials(
+        n_held, T, H, world, _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), _ptr(send), code, _stream(stream)))
+
+
+def dcp_lse_merge_packed(recv, world, n_held, lse_base, o, lse=None, wire_dtype=torch.bfloat16, stream=None):
+    """Merge the world * n_held parts of an all-to-all receive buffer (uint8 [world, chunk])
+    into o [rows, 512] (rows = T * H / world of this rank's heads) and lse [rows]."""
+    rows = o.numel() // 512
+    _dev(o, "o", o.dtype)
+    if o.shape[-1] != 512:
+        raise ValueError("o's last dim must be 512")
+    _dev(recv, "recv", torch.uint8)
+    code = DCP_BF16 if wire_dtype == torch.bfloat16 else DCP_F32
+    if rows:
+        e = 2 if code == DCP_BF16 else 4
+        need = n_held * rows * (512 * e + 4)
+        chunk = need + (-need % 256)
+        if recv.numel() != world * chunk:
+            raise ValueError(f"recv must hold world * chunk = {world * chunk} bytes")
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+        if lse.numel() != rows:
+            raise ValueError("lse must hold rows values")
+    _check("dcp_lse_merge_packed", load_library().dcp_lse_merge_packed(
+        world, n_held, rows, _ptr(recv), code, lse_base, _ptr(o), _dtype_code(o), _ptr(lse), _stream(stream)))
+
+
+def dcp_lse_rescale(lse_all, o_part, shard_begin, world, lse_base, o_sum, lse=None, stream=None):
+    """AllGather + ReduceScatter, local step: lse_all [n_shards, ..., H] f32 (every shard),
+    o_part [n_held, ..., H, 512] (this rank's shards) -> o_sum f32 [world, T, H / world, 512]
+    (and lse f32 [world, T, H / world])."""
+    n_shards, n_held, H = lse_all.shape[0], o_part.shape[0], o_part.shape[-2]
+    T = o_part.numel() // (n_held * H * 512) if o_part.numel() else 0
+    _dev(lse_all, "lse_all", torch.float32)
+    if lse_all.numel() != n_shards * T * H:
+        raise ValueError("lse_all must hold n_shards * T * H values")
+    _dev(o_part, "o_part", o_part.dtype)
+    _dev(o_sum, "o_sum", torch.float32)
+    if o_sum.numel() != T * H * 512:
+        raise ValueError("o_sum must hold T * H * 512 values")
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+        if lse.numel() != T * H:
+            raise ValueError("lse must hold T * H values")
+    _check("dcp_lse_rescale", load_library().dcp_lse_rescale(
+        n_shards, shard_begin, n_held, T, H, world, _ptr(lse_all), _ptr(o_part), _dtype_code(o_part), lse_base,
+        _ptr(o_sum), _ptr(lse), _stream(stream)))

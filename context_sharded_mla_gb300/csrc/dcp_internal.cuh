@@ -64,6 +64,81 @@ inline int32_t launch_status(int64_t launches = 1) {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// ---------------------------------------------------------------- 512-dim rows, one warp per row
+// Lane l owns the 16 dims [8l, 8l+8) and [256 + 8l, 256 + 8l + 8) of a 512-dim
+// row in every dtype (so f32 and bf16 rows agree on which lane holds which
+// dim); every warp access is one contiguous 1024-byte (f32) or 512-byte (bf16)
+// segment.  Rows must be 16-byte aligned.
+template <int kBf16>
+__device__ inline const void* row_ptr(const void* base, int64_t row) {
+  return static_cast<const unsigned char*>(base) + row * (int64_t)kDv * (kBf16 ? 2 : 4);
+}
+template <int kBf16>
+__device__ inline void* row_ptr(void* base, int64_t row) {
+  return static_cast<unsigned char*>(base) + row * (int64_t)kDv * (kBf16 ? 2 : 4);
+}
+
+template <int kInBf16>
+__device__ inline void load16(const void* row, int lane, float (&v)[16]) {
+  if (kInBf16) {
+    const uint4* p = static_cast<const uint4*>(row);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint4 u = __ldg(p + lane + 32 * j);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float2 f = __bfloat1622float2(h[k]);
+        v[8 * j + 2 * k] = f.x;
+        v[8 * j + 2 * k + 1] = f.y;
+      }
+    }
+  } else {
+    const float4* p = static_cast<const float4*>(row);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float4 a = __ldg(p + 2 * lane + 64 * j);
+      float4 b = __ldg(p + 2 * lane + 64 * j + 1);
+      v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = a.z; v[8 * j + 3] = a.w;
+      v[8 * j + 4] = b.x; v[8 * j + 5] = b.y; v[8 * j + 6] = b.z; v[8 * j + 7] = b.w;
+    }
+  }
+}
+
+template <int kOutBf16>
+__device__ inline void store16(void* row, int lane, const float (&v)[16]) {
+  if (kOutBf16) {
+    uint4* p = static_cast<uint4*>(row);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint4 u;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[8 * j + 2 * k], v[8 * j + 2 * k + 1]);
+      p[lane + 32 * j] = u;
+    }
+  } else {
+    float4* p = static_cast<float4*>(row);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      p[2 * lane + 64 * j] = make_float4(v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3]);
+      p[2 * lane + 64 * j + 1] = make_float4(v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- all-to-all wire format
+// One rank's send buffer holds, for each destination in turn, a chunk of
+// a2a_chunk_bytes: an o block [n_held][rows][512] (bf16 or f32) and, at
+// a2a_o_block_bytes, an lse block [n_held][rows] f32, padded to 256 bytes so
+// that every chunk starts aligned.  rows = query tokens x heads per destination.
+inline int64_t a2a_o_block_bytes(int64_t n_held, int64_t rows, int wire_bf16) {
+  return n_held * rows * kDv * (wire_bf16 ? 2 : 4);
+}
+inline int64_t a2a_chunk_bytes(int64_t n_held, int64_t rows, int wire_bf16) {
+  return (a2a_o_block_bytes(n_held, rows, wire_bf16) + n_held * rows * 4 + 255) & ~int64_t(255);
+}
+
 // cuTensorMapEncodeTiled from the driver, looked up once per process (nullptr if
 // unavailable).  The function-local static is initialised under the C++ runtime's
 // own lock, so concurrent first calls from several host threads are safe.

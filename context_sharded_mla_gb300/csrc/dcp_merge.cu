@@ -10,111 +10,103 @@
 // 16-byte vectors so that each warp access is one contiguous 1024-byte (f32) or
 // 512-byte (bf16) segment per part.  Algorithmic bytes per row:
 // n_parts * (512 * sizeof(o_part) + 4) read, 512 * sizeof(o) + 4 written.
+// The same kernel merges the parts of an all-to-all receive buffer in place
+// (dcp_lse_merge_packed): "Decode Context Parallelism" (zdszero), "通信策略",
+// all-to-all form: the receiver holds its heads' partials of every shard and
+// merges them locally.
 #include "dcp_internal.cuh"
 
 using namespace dcp;
 
 namespace {
 
-// Lane l owns the 16 dims [8l, 8l+8) and [256 + 8l, 256 + 8l + 8) in every
-// dtype, so the f32 and bf16 paths agree on which lane holds which dim.
-template <int kInBf16>
-__device__ inline void load16(const void* base, int64_t row, int lane, float (&v)[16]) {
-  if (kInBf16) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + row * kDv);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint4 u = __ldg(p + lane + 32 * j);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float2 f = __bfloat1622float2(h[k]);
-        v[8 * j + 2 * k] = f.x;
-        v[8 * j + 2 * k + 1] = f.y;
-      }
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kDv);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float4 a = __ldg(p + 2 * lane + 64 * j);
-      float4 b = __ldg(p + 2 * lane + 64 * j + 1);
-      v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = a.z; v[8 * j + 3] = a.w;
-      v[8 * j + 4] = b.x; v[8 * j + 5] = b.y; v[8 * j + 6] = b.z; v[8 * j + 7] = b.w;
-    }
+// Part r of merged row `row` in a dense [n_parts][rows] layout (dcp_lse_merge).
+struct DenseParts {
+  const void* o;
+  const float* lse;
+  int64_t rows;
+  template <int kBf16>
+  __device__ const void* o_row(int r, int64_t row) const {
+    return row_ptr<kBf16>(o, (int64_t)r * rows + row);
   }
-}
+  __device__ float lse_at(int r, int64_t row) const { return __ldg(lse + (int64_t)r * rows + row); }
+};
 
-template <int kOutBf16>
-__device__ inline void store16(void* base, int64_t row, int lane, const float (&v)[16]) {
-  if (kOutBf16) {
-    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row * kDv);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint4 u;
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[8 * j + 2 * k], v[8 * j + 2 * k + 1]);
-      p[lane + 32 * j] = u;
-    }
-  } else {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + row * kDv);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      p[2 * lane + 64 * j] = make_float4(v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3]);
-      p[2 * lane + 64 * j + 1] = make_float4(v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
-    }
+// Part r = w * n_held + s of merged row `row` in an all-to-all receive buffer
+// (dcp_lse_merge_packed): chunk w came from rank w and holds its o block
+// [n_held][rows][512] followed, at lse_off, by its lse block [n_held][rows].
+struct PackedParts {
+  const unsigned char* base;
+  int64_t chunk, lse_off, rows;
+  int32_t n_held;
+  template <int kBf16>
+  __device__ const void* o_row(int r, int64_t row) const {
+    const int w = r / n_held, s = r - w * n_held;
+    return row_ptr<kBf16>(base + w * chunk, (int64_t)s * rows + row);
   }
-}
+  __device__ float lse_at(int r, int64_t row) const {
+    const int w = r / n_held, s = r - w * n_held;
+    return __ldg(reinterpret_cast<const float*>(base + w * chunk + lse_off) + (int64_t)s * rows + row);
+  }
+};
 
-template <int kInBf16, int kOutBf16, int kBase2>
-__global__ void __launch_bounds__(256) lse_merge_kernel(int32_t n_parts, int64_t rows,
-                                                        const void* __restrict__ o_part,
-                                                        const float* __restrict__ lse_part,
+template <class Parts, int kInBf16, int kOutBf16, int kBase2>
+__global__ void __launch_bounds__(256) lse_merge_kernel(Parts parts, int32_t n_parts, int64_t rows,
                                                         void* __restrict__ o, float* __restrict__ lse) {
   const int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   // pass 1: m = max_r lse_r
   float m = -INFINITY;
-  for (int r = lane; r < n_parts; r += 32) m = fmaxf(m, __ldg(lse_part + (int64_t)r * rows + row));
+  for (int r = lane; r < n_parts; r += 32) m = fmaxf(m, parts.lse_at(r, row));
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   if (m == -INFINITY) {  // every part empty: the unit of the merge
-    store16<kOutBf16>(o, row, lane, acc);
+    store16<kOutBf16>(row_ptr<kOutBf16>(o, row), lane, acc);
     if (lse && lane == 0) lse[row] = -INFINITY;
     return;
   }
   // pass 2: weights relative to m, weighted sum of the partial outputs
   float wsum = 0.f;
   for (int r = 0; r < n_parts; ++r) {
-    const float l = __ldg(lse_part + (int64_t)r * rows + row);
+    const float l = parts.lse_at(r, row);
     if (l == -INFINITY) continue;  // zero weight; its o_r is not read
     const float w = kBase2 ? exp2f(l - m) : expf(l - m);
     wsum += w;
     float v[16];
-    load16<kInBf16>(o_part, (int64_t)r * rows + row, lane, v);
+    load16<kInBf16>(parts.template o_row<kInBf16>(r, row), lane, v);
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, v[i], acc[i]);
   }
   const float inv = 1.f / wsum;
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] *= inv;
-  store16<kOutBf16>(o, row, lane, acc);
+  store16<kOutBf16>(row_ptr<kOutBf16>(o, row), lane, acc);
   if (lse && lane == 0) lse[row] = m + (kBase2 ? log2f(wsum) : logf(wsum));
 }
 
-template <int kInBf16, int kOutBf16>
-void launch_merge(int base2, dim3 grid, cudaStream_t st, int32_t n, int64_t rows, const void* op,
-                  const float* lp, void* o, float* lse) {
-  if (base2)
-    lse_merge_kernel<kInBf16, kOutBf16, 1><<<grid, 256, 0, st>>>(n, rows, op, lp, o, lse);
-  else
-    lse_merge_kernel<kInBf16, kOutBf16, 0><<<grid, 256, 0, st>>>(n, rows, op, lp, o, lse);
+template <class Parts>
+int32_t launch_merge(const Parts& parts, int32_t n, int64_t rows, int in_bf16, int out_bf16, int base2, void* o,
+                     float* lse, void* stream) {
+  const int64_t blocks = (rows + 7) / 8;  // 8 rows (warps) per block
+  if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)blocks);
+  cudaStream_t st = as_stream(stream);
+  const int sel = in_bf16 * 4 + out_bf16 * 2 + base2;
+  switch (sel) {
+#define DCP_MERGE_CASE(I, O, B2) \
+  case I * 4 + O * 2 + B2: lse_merge_kernel<Parts, I, O, B2><<<grid, 256, 0, st>>>(parts, n, rows, o, lse); break;
+    DCP_MERGE_CASE(0, 0, 0) DCP_MERGE_CASE(0, 0, 1) DCP_MERGE_CASE(0, 1, 0) DCP_MERGE_CASE(0, 1, 1)
+    DCP_MERGE_CASE(1, 0, 0) DCP_MERGE_CASE(1, 0, 1) DCP_MERGE_CASE(1, 1, 0) DCP_MERGE_CASE(1, 1, 1)
+#undef DCP_MERGE_CASE
+  }
+  return launch_status();
 }
+
+bool dtype_ok(int32_t d) { return d == DCP_F32 || d == DCP_BF16; }
 
 }  // namespace
 
@@ -122,23 +114,27 @@ extern "C" int32_t dcp_lse_merge(int32_t n_parts, int64_t rows, const void* o_pa
                                  int32_t o_part_dtype, const float* lse_part, int32_t lse_base,
                                  void* o, int32_t o_dtype, float* lse, void* stream) {
   if (n_parts < 1 || rows < 0) return DCP_ERR_INVALID;
-  if ((o_part_dtype != DCP_F32 && o_part_dtype != DCP_BF16) || (o_dtype != DCP_F32 && o_dtype != DCP_BF16))
-    return DCP_ERR_INVALID;
+  if (!dtype_ok(o_part_dtype) || !dtype_ok(o_dtype)) return DCP_ERR_INVALID;
   if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2) return DCP_ERR_INVALID;
   if (rows == 0) return DCP_OK;
   if (!o_part || !lse_part || !o) return DCP_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(o_part) | reinterpret_cast<uintptr_t>(o)) & 15) return DCP_ERR_INVALID;
-  const int64_t blocks = (rows + 7) / 8;
-  if (blocks > INT32_MAX) return DCP_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)blocks);
-  cudaStream_t st = as_stream(stream);
-  const int b2 = lse_base == DCP_LSE_BASE_2;
-  if (o_part_dtype == DCP_BF16) {
-    if (o_dtype == DCP_BF16) launch_merge<1, 1>(b2, grid, st, n_parts, rows, o_part, lse_part, o, lse);
-    else launch_merge<1, 0>(b2, grid, st, n_parts, rows, o_part, lse_part, o, lse);
-  } else {
-    if (o_dtype == DCP_BF16) launch_merge<0, 1>(b2, grid, st, n_parts, rows, o_part, lse_part, o, lse);
-    else launch_merge<0, 0>(b2, grid, st, n_parts, rows, o_part, lse_part, o, lse);
-  }
-  return launch_status();
+  return launch_merge(DenseParts{o_part, lse_part, rows}, n_parts, rows, o_part_dtype == DCP_BF16,
+                      o_dtype == DCP_BF16, lse_base == DCP_LSE_BASE_2, o, lse, stream);
+}
+
+extern "C" int32_t dcp_lse_merge_packed(int32_t world, int32_t n_held, int64_t rows, const void* recv,
+                                        int32_t wire_dtype, int32_t lse_base, void* o, int32_t o_dtype, float* lse,
+                                        void* stream) {
+  if (world < 1 || n_held < 1 || rows < 0 || (int64_t)world * n_held > INT32_MAX) return DCP_ERR_INVALID;
+  if (!dtype_ok(wire_dtype) || !dtype_ok(o_dtype)) return DCP_ERR_INVALID;
+  if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2) return DCP_ERR_INVALID;
+  if (rows == 0) return DCP_OK;
+  if (!recv || !o) return DCP_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(recv) | reinterpret_cast<uintptr_t>(o)) & 15) return DCP_ERR_INVALID;
+  const int wire_bf16 = wire_dtype == DCP_BF16;
+  const PackedParts parts{static_cast<const unsigned char*>(recv), a2a_chunk_bytes(n_held, rows, wire_bf16),
+                          a2a_o_block_bytes(n_held, rows, wire_bf16), rows, n_held};
+  return launch_merge(parts, world * n_held, rows, wire_bf16, o_dtype == DCP_BF16, lse_base == DCP_LSE_BASE_2, o,
+                      lse, stream);
 }

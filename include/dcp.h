@@ -13,10 +13,17 @@
  * and, on either side of the attention, the two absorption products
  *   6. dcp_absorb_q            q_nope @ w_kc -> the 576-d absorbed query
  *   7. dcp_absorb_o            merged latent output @ w_vc -> per-head value
+ * and, when the shards are spread over W GPUs (one rank each), the two sides
+ * of the exchange of the partials
+ *   8. dcp_pack_partials       head slice d of every held shard -> rank d's chunk
+ *   9. dcp_lse_merge_packed    the head owner's merge, read from its receive buffer
+ *  10. dcp_lse_rescale         the local step of the AllGather + ReduceScatter form
  *
  * On one GPU the N context shards are N compact paged pools in one HBM
  * allocation (the "arena"), so the cross-rank steps (query all-gather,
- * all-to-all of the partials) become plain device buffers.
+ * all-to-all of the partials) become plain device buffers.  Over W GPUs each
+ * holds N / W consecutive shards; the caller runs the collective itself
+ * (e.g. NCCL all-to-all) between dcp_pack_partials and dcp_lse_merge_packed.
  *
  * Conventions for every entry point
  * ---------------------------------
@@ -377,6 +384,80 @@ int32_t dcp_absorb_q(int64_t T, int32_t H, const void* q_nope, int64_t q_nope_st
  */
 int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_dtype, const void* w_vc, void* v,
                      int32_t v_dtype, int32_t* status, void* stream);
+
+/*
+ * Exchange of the partials across W ranks (one GPU each).
+ *
+ * Sources: "Decode Context Parallelism" (zdszero), section "通信策略"
+ * ("合并：All-to-All": each rank cuts O_r by head into one piece per rank and
+ * sends it, with the matching LSE in the same buffer, to the rank that owns
+ * those heads, which merges locally; "合并：AllGather + ReduceScatter": gather
+ * every rank's LSE, correct each partial to exp(L_r - L) O_r, reduce-scatter the
+ * corrected partials by head); "MLA 的 Decode Context Parallelism", section 4,
+ * stages 6-7 and section 5 (the all-to-all carries bf16 o and an fp32 lse per
+ * row, about 6.3 MB per rank and step at B=64, H=96).
+ *
+ * Rank w of W holds shards [w * n_held, (w + 1) * n_held) (n_held = N / W) and
+ * owns heads [w * Hd, (w + 1) * Hd), Hd = H / W (H % W == 0).  Its partials are
+ * dcp_mla_decode_partial's outputs for its shards: o_part [n_held, T, H, 512]
+ * and lse_part [n_held, T, H], T = B * q_len query tokens.
+ *
+ * Wire format of the all-to-all: a send (or receive) buffer is [W][chunk],
+ * chunk = dcp_a2a_chunk_bytes(...) bytes; chunk d of a send buffer holds an o
+ * block [n_held, T, Hd, 512] in wire_dtype (bf16 rounded to nearest even, or
+ * f32) for heads [d * Hd, (d + 1) * Hd), then an lse block [n_held, T, Hd] f32
+ * right after the o block, padded to a multiple of 256 bytes.  After an
+ * all-to-all with equal chunks (chunk w of the receive buffer came from rank w)
+ * the receive buffer holds the head owner's rows of every shard in shard order.
+ */
+
+/* Bytes of one chunk (0 on bad arguments: n_held < 1, T < 0, H < 1, W < 1,
+ * H % W != 0, a bad dtype). */
+size_t dcp_a2a_chunk_bytes(int32_t n_held, int32_t T, int32_t H, int32_t world, int32_t wire_dtype);
+
+/*
+ * dcp_pack_partials — the send side of the all-to-all: chunk d of `send` gets
+ * head slice d of every held shard's o_part (converted to wire_dtype) and
+ * lse_part, in the wire format above.  o_part f32 or bf16 (o_part_dtype),
+ * 16-byte aligned; send [world * chunk] bytes, 16-byte aligned (256 keeps every
+ * chunk aligned).  Pad bytes are not written.  T == 0 is a no-op.  Errors:
+ * DCP_ERR_INVALID as for dcp_a2a_chunk_bytes, or a null / misaligned pointer.
+ */
+int32_t dcp_pack_partials(int32_t n_held, int32_t T, int32_t H, int32_t world, const void* o_part,
+                          int32_t o_part_dtype, const float* lse_part, void* send, int32_t wire_dtype,
+                          void* stream);
+
+/*
+ * dcp_lse_merge_packed — the receive side: the exact LSE merge (as
+ * dcp_lse_merge) of the world * n_held parts of each of `rows` = T * Hd rows,
+ * read in place from an all-to-all receive buffer `recv` [world * chunk] in the
+ * wire format (chunk w from rank w; part order = shard order).  o [rows, 512]
+ * f32 or bf16 (o_dtype), i.e. [T, Hd, 512] of this rank's heads; lse f32 [rows]
+ * in the partials' base (may be NULL).  rows == 0 is a no-op.  Errors:
+ * DCP_ERR_INVALID on bad sizes, dtypes or base, or a null / misaligned pointer.
+ */
+int32_t dcp_lse_merge_packed(int32_t world, int32_t n_held, int64_t rows, const void* recv, int32_t wire_dtype,
+                             int32_t lse_base, void* o, int32_t o_dtype, float* lse, void* stream);
+
+/*
+ * dcp_lse_rescale — the local step of the AllGather + ReduceScatter form.
+ *
+ *   lse_all   f32 [n_shards, T, H]: every shard's lse, shard order (the
+ *             all-gather of each rank's lse_part)
+ *   o_part    this rank's partials [n_held, T, H, 512], f32 or bf16
+ *   o_sum     (out) f32 [world, T, Hd, 512]: block d, row (t, h') holds
+ *             sum_{s held} base^(lse_{shard_begin+s} - L) * o_part[s, t, d*Hd + h']
+ *             with L = log sum_r base^lse_r over all n_shards (the row's merged
+ *             lse); a reduce-scatter (sum) of o_sum over the ranks leaves rank d
+ *             the merged o of its heads
+ *   lse       (out, may be NULL) f32 [world, T, Hd]: L in the same layout
+ * A row whose shards are all empty gets o_sum = 0 and L = -inf.  T == 0 is a
+ * no-op.  Errors: DCP_ERR_INVALID on bad sizes (shard_begin + n_held >
+ * n_shards, H % world != 0, ...), dtype or base, or a null / misaligned pointer.
+ */
+int32_t dcp_lse_rescale(int32_t n_shards, int32_t shard_begin, int32_t n_held, int32_t T, int32_t H, int32_t world,
+                        const float* lse_all, const void* o_part, int32_t o_part_dtype, int32_t lse_base,
+                        float* o_sum, float* lse, void* stream);
 
 #ifdef __cplusplus
 }
