@@ -252,18 +252,14 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
             st_shared_v4(srow + 128 * c + 16 * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
         }
       };
-      // Two register buffers: the TMEM load of the next 32 columns is in flight
-      // while the current ones are converted and staged.  NT / 32 is even.
-      uint32_t ra[32], rb[32];
-      tmem_ld32(lane_addr, ra);
+      // 32 columns at a time; each load completes inside its own asm statement
+      // (a load left in flight across other work could have its registers
+      // copied before they are filled).
+      uint32_t ra[32];
 #pragma unroll 1
-      for (int c = 0; c < NT / 32; c += 2) {
-        tmem_ld_wait_regs(ra);
-        tmem_ld32(lane_addr + 32 * (c + 1), rb);
+      for (int c = 0; c < NT / 32; ++c) {
+        tmem_ld32_sync(lane_addr + 32 * c, ra);
         stage_chunk(c, ra);
-        tmem_ld_wait_regs(rb);
-        if (c + 2 < NT / 32) tmem_ld32(lane_addr + 32 * (c + 2), ra);
-        stage_chunk(c + 1, rb);
       }
       // The warp then writes its own 32 staged rows out, one row segment per
       // coalesced store (16 bytes per lane).

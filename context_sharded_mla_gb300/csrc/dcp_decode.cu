@@ -301,13 +301,12 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
     uint32_t r[32];
-    tmem_ld16x2<128>(o_addr + 32 * k, r);
-    tmem_ld_wait();
+    tmem_ld16x2_sync<128>(o_addr + 32 * k, r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
     tmem_st16x2<128>(o_addr + 32 * k, r);
+    tmem_st_wait();  // before the next load reuses r
   }
-  tmem_st_wait();
 }
 
 // v[idx] for idx in 0..3, without indexing registers at run time
@@ -323,19 +322,19 @@ __device__ __forceinline__ uint32_t sel4(uint32_t v0, uint32_t v1, uint32_t v2, 
 //
 // fp32 rows: per 32 dims, the four lanes of each lane group (4 rows) trade
 // 32-byte blocks by shuffles (each lane offers a rotated block, then picks)
-// so that the group writes 128 contiguous bytes of one row per store: 8 lines
-// per warp store instead of 32.  bf16 rows: 32-byte stores, one row per lane.
+// so that the group writes 128 contiguous bytes of one row per pair of stores.
+// bf16 rows: one row per lane.  All stores are 16 bytes wide: a 32-byte
+// st.global.v8 in this routine was found to land only its first word in one
+// build of the kernel.
 __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int rows_here, bool whole,
                                           int64_t out_base, int64_t piece_base, int r0, int d0, float inv) {
   const int lane = threadIdx.x & 31;
   const int row = r0 + (lane & 15);
   if (whole && a.o_bf16) {
-    const bool wide = (reinterpret_cast<uintptr_t>(a.o_part) & 31) == 0;
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
       uint32_t rr[32];
-      tmem_ld16x2<128>(o_addr + 32 * k, rr);
-      tmem_ld_wait();
+      tmem_ld16x2_sync<128>(o_addr + 32 * k, rr);
       if (row >= rows_here) continue;
       uint32_t w[16];
 #pragma unroll
@@ -343,26 +342,18 @@ __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int 
         __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
         w[e] = *reinterpret_cast<uint32_t*>(&hh);
       }
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_part) + (out_base + row) * kDv + d0 + 32 * k;
-      if (wide) {
-        st_global_v8(dst, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
-        st_global_v8(dst + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
-      } else {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+      uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + (out_base + row) * kDv + d0 + 32 * k);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
     return;
   }
   float* const out0 = whole ? static_cast<float*>(a.o_part) + out_base * kDv : a.piece_o + piece_base * kDv;
-  const bool wide = (reinterpret_cast<uintptr_t>(out0) & 31) == 0;  // pieces are 256-byte aligned
   const int p = lane & 3, gl = lane & ~3;
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
     uint32_t rr[32];
-    tmem_ld16x2<128>(o_addr + 32 * k, rr);
-    tmem_ld_wait();
+    tmem_ld16x2_sync<128>(o_addr + 32 * k, rr);
 #pragma unroll
     for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * inv);
     // step s: lane p offers its block (p + s) & 3 and takes block p of lane (p - s) & 3
@@ -382,14 +373,9 @@ __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int 
 #pragma unroll
       for (int w = 0; w < 8; ++w) v8[w] = sel4(got[0][w], got[1][w], got[2][w], got[3][w], s);
       if (rq < rows_here) {
-        float* dst = out0 + (int64_t)rq * kDv + d0 + 32 * k + 8 * p;
-        if (wide) {
-          st_global_v8(dst, v8);
-        } else {
-          float4* d4 = reinterpret_cast<float4*>(dst);
-          d4[0] = make_float4(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]), __uint_as_float(v8[3]));
-          d4[1] = make_float4(__uint_as_float(v8[4]), __uint_as_float(v8[5]), __uint_as_float(v8[6]), __uint_as_float(v8[7]));
-        }
+        float4* d4 = reinterpret_cast<float4*>(out0 + (int64_t)rq * kDv + d0 + 32 * k + 8 * p);
+        d4[0] = make_float4(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]), __uint_as_float(v8[3]));
+        d4[1] = make_float4(__uint_as_float(v8[4]), __uint_as_float(v8[5]), __uint_as_float(v8[6]), __uint_as_float(v8[7]));
       }
     }
   }
@@ -878,8 +864,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t s[32];  // score bits, keys [32 h, 32 h + 32)
           if (!wwait(&bars[kSFull0 + bsel], (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          tmem_ld16x2<32>(tmem + lane_addr + kSCol + kTile * bsel, s);
-          tmem_ld_wait();
+          tmem_ld16x2_sync<32>(tmem + lane_addr + kSCol + kTile * bsel, s);
           send(j, s);
           tc_fence_before();
           __syncwarp();
