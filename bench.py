@@ -519,6 +519,13 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
     q = torch.empty(cfg.B, cfg.q_len, H, 576, dtype=torch.bfloat16, device=device)
     v = torch.empty(cfg.B, cfg.q_len, H, 128, dtype=torch.bfloat16, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
+    # the decode step's partials at these shapes (f32, N parts), for the merge and
+    # the fused merge + output product
+    o_part = torch.randn(cfg.N, T, H, 512, generator=g, device=device)
+    lse_part = torch.randn(cfg.N, T, H, generator=g, device=device)
+    o_merged = torch.empty(T, H, 512, dtype=o_dtype, device=device)
+    lse_merged = torch.empty(T, H, dtype=torch.float32, device=device)
+    base = dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_sum = torch.empty((), dtype=torch.float32, device=device)
     q_bytes, o_bytes = absorb_bytes(T, H, o.element_size(), 2)
@@ -543,7 +550,7 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
     time.sleep(0.3)
     barrier(dist)
     launches0 = dcp.dcp_launch_count()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     torch.cuda.profiler.start()
     clocks.mark()
     # The kernels take microseconds, less than the host needs to submit them:
@@ -557,6 +564,15 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
         ev[i][1].record(stream)
         dcp.dcp_absorb_o(o, w_vc, v, status)
         ev[i][2].record(stream)
+        flush_l2()
+        ev[i][3].record(stream)
+        dcp.dcp_lse_merge(o_part.view(cfg.N, -1, 512), lse_part.view(cfg.N, -1), base, o_merged.view(-1, 512),
+                          lse_merged.view(-1))
+        ev[i][4].record(stream)
+        flush_l2()
+        ev[i][5].record(stream)
+        dcp.dcp_lse_merge_absorb_o(o_part, lse_part, base, w_vc, v.view(T, H, 128), lse_merged, status)
+        ev[i][6].record(stream)
     barrier(dist)
     clocks.mark()
     torch.cuda.profiler.stop()
@@ -566,6 +582,8 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
         raise RuntimeError(f"device status {int(status.item())} after the timed absorption products")
     q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     o_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    merge_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in ev)
+    fused = [e[5].elapsed_time(e[6]) for e in ev]
     ms = max_over_ranks(dist, q_ms + o_ms)
     peaks = load_peaks()
     dom = ("absorb_kernel (query side)", q_bytes, q_ms) if q_ms >= o_ms else ("absorb_kernel (output side)",
@@ -613,7 +631,14 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
                                f"w_kc [H,128,512], w_vc [H,512,128], o {str(o_dtype).split('.')[-1]}, v bf16",
                    "T": T, "H": H, "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB written and "
                                           "read back, outside the timed kernels)"},
-        "kernels_us": {"absorb_q": round(q_ms * 1e3, 3), "absorb_o": round(o_ms * 1e3, 3)},
+        "kernels_us": {"absorb_q": round(q_ms * 1e3, 3), "absorb_o": round(o_ms * 1e3, 3),
+                       "lse_merge": round(merge_ms * 1e3, 3),
+                       "lse_merge_absorb_o": round(statistics.mean(fused) * 1e3, 3)},
+        "products_step_cost_us": {
+            "separate": round((q_ms + o_ms) * 1e3, 3),
+            "fused": round((q_ms + statistics.mean(fused) - merge_ms) * 1e3, 3),
+            "note": "what the two products add to a decode step: absorb_q + absorb_o after a separate merge, or "
+                    "absorb_q + (fused merge-and-product - plain merge); N f32 partials, L2 flushed before each call"},
         "bytes_alg": {"absorb_q": q_bytes, "absorb_o": o_bytes},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

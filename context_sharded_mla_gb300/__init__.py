@@ -10,8 +10,8 @@ works but the first call raises ``RuntimeError``.
 Functions (same names as the C ABI):
   dcp_count, dcp_slot_map, dcp_kv_append, dcp_mla_decode_partial,
   dcp_mla_decode_workspace_size, dcp_lse_merge, dcp_kv_relayout, dcp_absorb_q,
-  dcp_absorb_o, dcp_a2a_chunk_bytes, dcp_pack_partials, dcp_lse_merge_packed,
-  dcp_lse_rescale
+  dcp_absorb_o, dcp_lse_merge_absorb_o, dcp_a2a_chunk_bytes, dcp_pack_partials,
+  dcp_lse_merge_packed, dcp_lse_rescale
 """
 
 from __future__ import annotations
@@ -28,7 +28,7 @@ __all__ = [
     "dcp_count", "dcp_slot_map", "dcp_kv_append", "dcp_mla_decode_partial",
     "dcp_mla_decode_workspace_size", "dcp_lse_merge", "dcp_launch_count", "dcp_kv_relayout",
     "dcp_mla_decode_partial_static", "dcp_mla_decode_static_scratch_bytes", "dcp_absorb_q", "dcp_absorb_o",
-    "dcp_a2a_chunk_bytes", "dcp_pack_partials", "dcp_lse_merge_packed", "dcp_lse_rescale",
+    "dcp_a2a_chunk_bytes", "dcp_pack_partials", "dcp_lse_merge_packed", "dcp_lse_rescale", "dcp_lse_merge_absorb_o",
     "DCP_LSE_BASE_E", "DCP_LSE_BASE_2", "DCP_F32", "DCP_BF16", "STATUS_BITS",
 ]
 
@@ -78,6 +78,7 @@ _SIGNATURES = {
     "dcp_mla_decode_static_scratch_bytes": (_SZ, []),
     "dcp_absorb_q": (_I32, [_I64, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "dcp_absorb_o": (_I32, [_I64, _I32, _P, _I32, _P, _P, _I32, _P, _P]),
+    "dcp_lse_merge_absorb_o": (_I32, [_I32, _I64, _I32, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P]),
     "dcp_a2a_chunk_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "dcp_pack_partials": (_I32, [_I32, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P]),
     "dcp_lse_merge_packed": (_I32, [_I32, _I32, _I64, _P, _I32, _I32, _P, _I32, _P, _P]),
@@ -343,6 +344,32 @@ def dcp_absorb_o(o, w_vc, v, status=None, stream=None):
     T = o.numel() // (H * 512)
     _check("dcp_absorb_o", load_library().dcp_absorb_o(
         T, H, _ptr(o), _dtype_code(o), _ptr(w_vc), _ptr(v), _dtype_code(v), _ptr(status), _stream(stream)))
+
+
+def dcp_lse_merge_absorb_o(o_part, lse_part, lse_base, w_vc, v, lse=None, status=None, stream=None):
+    """v [..., H, 128] = bf16(LSE merge of o_part [n, ..., H, 512] / lse_part [n, ..., H]) @ w_vc[h];
+    lse [..., H] gets the merged lse (optional).  One kernel; the merged o is not written."""
+    n, H = o_part.shape[0], w_vc.shape[0]
+    _dev(w_vc, "w_vc", torch.bfloat16, (H, 512, 128))
+    _dev(o_part, "o_part", o_part.dtype)
+    if o_part.shape[-1] != 512 or o_part.shape[-2] != H:
+        raise ValueError(f"o_part must be [n, ..., {H}, 512]")
+    T = o_part.numel() // (n * H * 512)
+    _dev(lse_part, "lse_part", torch.float32)
+    if lse_part.numel() != n * T * H:
+        raise ValueError("lse_part must hold n * T * H values")
+    _dev(v, "v", v.dtype)
+    if v.numel() != T * H * 128 or v.shape[-1] != 128:
+        raise ValueError("v must be [..., H, 128] with T * H rows")
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+        if lse.numel() != T * H:
+            raise ValueError("lse must hold T * H values")
+    if status is not None:
+        _dev(status, "status", torch.int32, (1,))
+    _check("dcp_lse_merge_absorb_o", load_library().dcp_lse_merge_absorb_o(
+        n, T, H, _ptr(o_part), _dtype_code(o_part), _ptr(lse_part), lse_base, _ptr(w_vc), _ptr(v), _dtype_code(v),
+        _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def dcp_a2a_chunk_bytes(n_held, T, H, world, wire_dtype=torch.bfloat16) -> int:

@@ -291,6 +291,240 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   if (warp == kIssuerWarp) tmem_dealloc(tmem, NT);
 }
 
+// ---------------------------------------------------------------------------- merge + output product
+// The LSE merge of the N partials and the output-side product in one kernel
+// ("MLA 的 Decode Context Parallelism", section 4, stage 7: the two-pass merge
+// and the w_vc up-projection at the head owner): per head h and 16 query
+// tokens, the merged latent output o[t, h, :] is formed in shared memory as a
+// bf16 operand and multiplied by w_vc[h] on the tensor core; only v (and the
+// merged lse) is written.  The merged o never reaches global memory.
+// The product is computed transposed, v^T = w_vc[h]^T o^T: A = w_vc[h] as an
+// MN-major [128 n][64 k] operand per K-step (straight from its [k][n] rows by
+// TMA), B = the merged rows as a K-major [16 tokens][64 k] operand, D = 128
+// TMEM lanes (output dims) x 16 columns (tokens).  So no operand rows are
+// padding, a CTA needs about 90 KB of shared memory (two per SM), and the
+// epilogue writes each token's 128 outputs as one coalesced row.
+//   warps 0-7   merge: row weights w_p = base^(lse_p - m) / Z (m = max_p lse_p),
+//               then every row's 512 dims as sum_p w_p o_p, rounded to bf16 into
+//               eight 128-byte-swizzled K-major tiles [16 rows][64 k]; warps
+//               0-3 then run the epilogue (warp w: output dims 32w .. 32w + 31)
+//   warp 8      TMA producer: w_vc[h] K-step by K-step, 4 stages
+//   warp 9      TMEM owner and MMA issuer: M=128, N=16, K=16 products
+// HBM-bound: the partials (N * 512 * 4 bytes per row in f32) are read once;
+// w_vc[h] (128 KB) is read once per 16 tokens, mostly from L2.
+constexpr int kMaThreads = 320;
+constexpr int kMaMergeWarps = 8;
+constexpr int kMaProducerWarp = 8;
+constexpr int kMaIssuerWarp = 9;
+constexpr int kMaTok = 16;                    // query tokens per CTA (the product's N)
+constexpr int kMaKSteps = kDv / kKStep;       // 8
+constexpr int kMaWStages = 4;
+constexpr int kMaMaxParts = 64;
+constexpr uint32_t kMaBTileBytes = kMaTok * 128;                             // [16 rows][64 k] bf16, 2 KB
+constexpr uint32_t kMaWStageBytes = 2 * kWBoxBytes;                          // [64 k][128 n] bf16, 16 KB
+constexpr uint32_t kMaW = 0;                                                 // 4 W stages, 64 KB
+constexpr uint32_t kMaB = kMaW + kMaWStages * kMaWStageBytes;                // 8 B tiles, 16 KB
+constexpr uint32_t kMaWts = kMaB + kMaKSteps * kMaBTileBytes;                // weights [parts][16] f32, 4 KB
+constexpr uint32_t kMaBars = kMaWts + kMaMaxParts * kMaTok * 4;              // full[4], empty[4], b_ready, done
+constexpr uint32_t kMaMisc = kMaBars + (2 * kMaWStages + 2) * 8;
+constexpr uint32_t kMaBytes = kMaMisc + 16 + 1024;                            // + alignment slack
+
+struct MergeAbsorbArgs {
+  int64_t T;
+  int32_t H, n_parts, base2;
+  const void* o_part;     // [n_parts, T, H, 512] f32 or bf16
+  const float* lse_part;  // [n_parts, T, H]
+  void* v;                // [T, H, 128] f32 or bf16
+  int32_t v_bf16;
+  float* lse;             // [T, H] or null
+  int32_t* status;
+};
+
+template <int kInBf16>
+__device__ __forceinline__ float4 load_part4(const void* base, int64_t elem) {
+  if (kInBf16) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem));
+}
+
+template <int kInBf16, int kBase2>
+__global__ void __launch_bounds__(kMaThreads, 2)
+    merge_absorb_kernel(const __grid_constant__ CUtensorMap tmap_w, MergeAbsorbArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* wts = reinterpret_cast<float*>(smem + kMaWts);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMaBars);
+  uint64_t* empty = full + kMaWStages;
+  uint64_t* b_ready = empty + kMaWStages;
+  uint64_t* done = b_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMaMisc);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kMaMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;
+  const int64_t t0 = (int64_t)blockIdx.y * kMaTok;
+
+  auto issue_w = [&](int ks) {
+    const int s = ks % kMaWStages;
+    uint8_t* st = smem + kMaW + s * kMaWStageBytes;
+    mbar_arrive_expect_tx(&full[s], kMaWStageBytes);
+    tma_load_3d(st, &tmap_w, &full[s], 0, ks * kKStep, h);
+    tma_load_3d(st + kWBoxBytes, &tmap_w, &full[s], 64, ks * kKStep, h);
+  };
+  if (warp == kMaProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_w);
+    for (int s = 0; s < kMaWStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(b_ready, kMaMergeWarps);
+    mbar_init(done, 1);
+    *abort_s = 0;
+    fence_barrier_init();
+    for (int ks = 0; ks < kMaWStages; ++ks) issue_w(ks);  // w_vc[h] starts streaming at once
+  }
+  if (warp == kMaIssuerWarp) {
+    tmem_alloc(tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kMaProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int ks = kMaWStages; ks < kMaKSteps; ++ks) {
+        if (!mbar_wait(&empty[ks % kMaWStages], ((ks / kMaWStages) - 1) & 1, abort_s)) break;
+        issue_w(ks);
+      }
+    }
+  } else if (warp == kMaIssuerWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kMaTok, 1, 0);  // A = w_vc MN-major, B = o K-major
+      bool ok = mbar_wait(b_ready, 0, abort_s);
+      for (int ks = 0; ks < kMaKSteps && ok; ++ks) {
+        const int s = ks % kMaWStages;
+        if (!mbar_wait(&full[s], (ks / kMaWStages) & 1, abort_s)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t wdesc = sw128_desc(smem_u32(smem + kMaW + s * kMaWStageBytes), kWBoxBytes, 1024);
+        const uint64_t bdesc = sw128_desc(smem_u32(smem + kMaB + ks * kMaBTileBytes), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kKStep / 16; ++kk)
+          mma_bf16_ss(tmem, wdesc + kk * (2048 >> 4), bdesc + kk * (32 >> 4), idesc, (ks | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      if (ok) mma_commit(done);
+    }
+  } else {
+    // ------------------------------------------------------------------ merge warps 0-7, then the epilogue
+    constexpr int kMergeThreads = 32 * kMaMergeWarps;
+    // row weights: all parts' lse of the 16 tokens land in shared memory at once
+    // (one load per thread), then thread r < 16 of warp 0 turns token t0 + r's
+    // into weights
+    const int64_t rows = a.T * a.H;
+    for (int i = tid; i < a.n_parts * kMaTok; i += kMergeThreads) {
+      const int p = i / kMaTok, r = i % kMaTok;
+      const int64_t t = t0 + r;
+      wts[i] = t < a.T ? __ldg(a.lse_part + p * rows + t * a.H + h) : -INFINITY;
+    }
+    named_bar_sync(1, kMergeThreads);
+    if (warp == 0 && lane < kMaTok) {
+      const int64_t t = t0 + lane;
+      float m = -INFINITY;
+      for (int p = 0; p < a.n_parts; ++p) m = fmaxf(m, wts[p * kMaTok + lane]);
+      float z = 0.f;
+      for (int p = 0; p < a.n_parts; ++p) {
+        const float l = wts[p * kMaTok + lane];
+        const float w = (m == -INFINITY || l == -INFINITY) ? 0.f : (kBase2 ? exp2f(l - m) : expf(l - m));
+        wts[p * kMaTok + lane] = w;
+        z += w;
+      }
+      const float inv = z > 0.f ? 1.f / z : 0.f;
+      for (int p = 0; p < a.n_parts; ++p) wts[p * kMaTok + lane] *= inv;
+      if (t < a.T && a.lse) a.lse[t * a.H + h] = z > 0.f ? m + (kBase2 ? log2f(z) : logf(z)) : -INFINITY;
+    }
+    named_bar_sync(1, kMergeThreads);
+    // merged rows: float4 f = tid + 256 i (i < 8) is row f / 128, dims 4 (f % 128) .. + 4
+    {
+      constexpr int kPer = kMaTok * (kDv / 4) / kMergeThreads;  // 8
+      float4 acc[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+      for (int p = 0; p < a.n_parts; ++p) {
+        float4 x[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int f = tid + kMergeThreads * i, r = f >> 7, c = f & 127;
+          const int64_t t = t0 + r;
+          x[i] = (t < a.T && wts[p * kMaTok + r] != 0.f)
+                     ? load_part4<kInBf16>(a.o_part, ((int64_t)p * rows + t * a.H + h) * kDv + 4 * c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int f = tid + kMergeThreads * i, r = f >> 7;
+          const float w = wts[p * kMaTok + r];
+          acc[i].x = fmaf(w, x[i].x, acc[i].x);
+          acc[i].y = fmaf(w, x[i].y, acc[i].y);
+          acc[i].z = fmaf(w, x[i].z, acc[i].z);
+          acc[i].w = fmaf(w, x[i].w, acc[i].w);
+        }
+      }
+      // bf16 into the swizzled K-major tiles: 16-byte chunk c16 of row r sits at
+      // r * 128 + ((c16 ^ (r % 8)) * 16) of K-step tile c / 16
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int f = tid + kMergeThreads * i, r = f >> 7, c = f & 127;
+        const int ks = c >> 4, c4 = c & 15;
+        const uint32_t off = kMaB + ks * kMaBTileBytes + r * 128 + (((c4 >> 1) ^ (r & 7)) << 4) + (c4 & 1) * 8;
+        st_shared_v2(smem_u32(smem) + off, pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_ready);
+    if (warp < 4) {
+      // epilogue: TMEM lane 32w + l holds output dim 32w + l for the 16 tokens
+      // (columns).  The TMEM load is warp-collective (.sync.aligned): every lane
+      // of the warp runs it; only the stores depend on the token being live.
+      const bool ok = warp_wait_all(done, 0, abort_s);  // warp-uniform
+      tc_fence_after();
+      if (ok) {
+        uint32_t r[16];
+        tmem_ld32x16_sync(tmem + ((uint32_t)(32 * warp) << 16), r);
+        const int n = 32 * warp + lane;
+#pragma unroll
+        for (int j = 0; j < kMaTok; ++j) {
+          const int64_t t = t0 + j;
+          if (t >= a.T) break;
+          if (a.v_bf16)
+            static_cast<__nv_bfloat16*>(a.v)[(t * a.H + h) * 128 + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
+          else
+            static_cast<float*>(a.v)[(t * a.H + h) * 128 + n] = __uint_as_float(r[j]);
+        }
+      }
+    }
+  }
+
+  if (*abort_s && tid == 0) flag(a.status, DCP_STATUS_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_s) __nanosleep(100000);
+  tc_fence_after();
+  if (warp == kMaIssuerWarp) tmem_dealloc(tmem, 32);
+}
+
 // bf16 A rows of K elements: dims (k, head, token), box [128 tokens][1][64 k].
 bool make_tmap_a(CUtensorMap* m, const void* base, int64_t K, int64_t H, int64_t T, int64_t row_stride) {
   auto enc = tmap_encoder();
@@ -386,4 +620,49 @@ extern "C" int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_d
   a.a_f32 = reinterpret_cast<const float*>(o);
   a.a_f32_stride = kDv;
   return launch<kOTile, 8, kOStages, false, true>(tw, tw, a, 128 / kOTile, as_stream(stream));
+}
+
+namespace {
+
+template <int kInBf16, int kBase2>
+int32_t launch_merge_absorb(const CUtensorMap& tw, const MergeAbsorbArgs& a, cudaStream_t st) {
+  static SmemLimit limit;
+  if (!limit.ensure(reinterpret_cast<const void*>(&merge_absorb_kernel<kInBf16, kBase2>), kMaBytes))
+    return DCP_ERR_CUDA;
+  const dim3 grid((unsigned)a.H, (unsigned)((a.T + kMaTok - 1) / kMaTok));
+  merge_absorb_kernel<kInBf16, kBase2><<<grid, kMaThreads, kMaBytes, st>>>(tw, a);
+  return launch_status();
+}
+
+}  // namespace
+
+extern "C" int32_t dcp_lse_merge_absorb_o(int32_t n_parts, int64_t T, int32_t H, const void* o_part,
+                                          int32_t o_part_dtype, const float* lse_part, int32_t lse_base,
+                                          const void* w_vc, void* v, int32_t v_dtype, float* lse, int32_t* status,
+                                          void* stream) {
+  if (n_parts < 1 || n_parts > kMaMaxParts || T < 0 || H < 1 || H > 65535 || (T + kMaTok - 1) / kMaTok > 65535)
+    return DCP_ERR_INVALID;
+  if ((o_part_dtype != DCP_F32 && o_part_dtype != DCP_BF16) || (v_dtype != DCP_F32 && v_dtype != DCP_BF16))
+    return DCP_ERR_INVALID;
+  if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2) return DCP_ERR_INVALID;
+  if (T == 0) return DCP_OK;
+  if (!o_part || !lse_part || !w_vc || !v) return DCP_ERR_INVALID;
+  if (!aligned16(o_part) || !aligned16(w_vc) || !aligned16(v)) return DCP_ERR_INVALID;
+  CUtensorMap tw;
+  if (!make_tmap_w(&tw, w_vc, H, kDv, 128)) return DCP_ERR_CUDA;
+  MergeAbsorbArgs a{};
+  a.T = T;
+  a.H = H;
+  a.n_parts = n_parts;
+  a.base2 = lse_base == DCP_LSE_BASE_2;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.v = v;
+  a.v_bf16 = v_dtype == DCP_BF16;
+  a.lse = lse;
+  a.status = status;
+  cudaStream_t st = as_stream(stream);
+  const bool ib = o_part_dtype == DCP_BF16;
+  if (ib) return a.base2 ? launch_merge_absorb<1, 1>(tw, a, st) : launch_merge_absorb<1, 0>(tw, a, st);
+  return a.base2 ? launch_merge_absorb<0, 1>(tw, a, st) : launch_merge_absorb<0, 0>(tw, a, st);
 }

@@ -13,6 +13,7 @@
  * and, on either side of the attention, the two absorption products
  *   6. dcp_absorb_q            q_nope @ w_kc -> the 576-d absorbed query
  *   7. dcp_absorb_o            merged latent output @ w_vc -> per-head value
+ *      dcp_lse_merge_absorb_o  the merge and that product in one kernel
  * and, when the shards are spread over W GPUs (one rank each), the two sides
  * of the exchange of the partials
  *   8. dcp_pack_partials       head slice d of every held shard -> rank d's chunk
@@ -384,6 +385,32 @@ int32_t dcp_absorb_q(int64_t T, int32_t H, const void* q_nope, int64_t q_nope_st
  */
 int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_dtype, const void* w_vc, void* v,
                      int32_t v_dtype, int32_t* status, void* stream);
+
+/*
+ * dcp_lse_merge_absorb_o — the LSE merge and the output-side absorption
+ * product in one call: v[t, h] = bf16(merged o[t, h]) @ w_vc[h].
+ *
+ * Sources: as dcp_lse_merge (the merge) and dcp_absorb_o (identity 2); "MLA 的
+ * Decode Context Parallelism", section 4, stage 7 (the head owner merges the
+ * partials and applies the V up-projection w_vc).  The merged latent output is
+ * formed in shared memory as the tensor core's operand and never written out.
+ *
+ *   o_part    [n_parts, T, H, 512] f32 or bf16 (o_part_dtype): the partials,
+ *             e.g. dcp_mla_decode_partial's o_part with T = B * q_len
+ *   lse_part  f32 [n_parts, T, H] in base e (lse_base 0) or base 2 (1)
+ *   w_vc      bf16 [H, 512, 128]
+ *   v   (out) [T, H, 128] f32 or bf16 (v_dtype): f32 accumulation of the merged
+ *             o, rounded to nearest bf16, times w_vc[h]
+ *   lse (out) f32 [T, H], the merged lse in the partials' base (may be NULL)
+ *   status    device word (may be NULL); DCP_STATUS_TIMEOUT if a pipeline wait
+ *             gave up (v is then invalid)
+ * A row whose parts are all empty gives v = 0 and lse = -inf.  T == 0 is a
+ * no-op.  Errors: DCP_ERR_INVALID on n_parts outside [1, 64], T < 0, H outside
+ * [1, 65535], a bad dtype or base, or a null / misaligned (16-byte) pointer.
+ */
+int32_t dcp_lse_merge_absorb_o(int32_t n_parts, int64_t T, int32_t H, const void* o_part, int32_t o_part_dtype,
+                               const float* lse_part, int32_t lse_base, const void* w_vc, void* v, int32_t v_dtype,
+                               float* lse, int32_t* status, void* stream);
 
 /*
  * Exchange of the partials across W ranks (one GPU each).
