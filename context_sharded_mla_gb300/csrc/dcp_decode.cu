@@ -160,10 +160,18 @@ __device__ inline int64_t unit_nvis_max(const TcArgs& a, int b, int rs, bool* ba
 }
 
 // ---------------------------------------------------------------------------- planner
+// Tile prefix sums of the (request, shard) units, and the rows of units with no
+// visible key (an empty shard): o = 0 and lse = -inf, written here because the
+// main kernel never visits them.  One block of 1024 threads, 1024 units per pass.
 __global__ void __launch_bounds__(1024) plan_kernel(TcArgs a, int32_t* tile_start, int32_t U) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
-  if (threadIdx.x == 0) carry = 0;
+  __shared__ int32_t empty_s[1024];
+  __shared__ int32_t n_empty_s;
+  if (threadIdx.x == 0) {
+    carry = 0;
+    n_empty_s = 0;
+  }
   __syncthreads();
   for (int32_t base = 0; base < U; base += 1024) {
     const int32_t u = base + threadIdx.x;
@@ -174,6 +182,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(TcArgs a, int32_t* tile_star
       const int64_t n = unit_nvis_max(a, b, rs, &bad);
       if (bad && rs == 0) flag(a.status, DCP_STATUS_BAD_LENGTH);
       t = (int32_t)((n + kTile - 1) / kTile);
+      if (t == 0) empty_s[atomicAdd(&n_empty_s, 1)] = u;  // at most 1024 per pass
     }
     // block-wide inclusive scan
     int32_t x = t;
@@ -199,6 +208,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(TcArgs a, int32_t* tile_star
     if (u < U) tile_start[u] = incl - t;
     __syncthreads();
     if (threadIdx.x == 1023) carry = incl;
+    // this pass's empty units: every thread writes 16-byte pieces of their rows
+    const int n_empty = n_empty_s;
+    const int64_t row_bytes = (int64_t)kDv * (a.o_bf16 ? 2 : 4);
+    for (int k = 0; k < n_empty; ++k) {
+      const int32_t ue = empty_s[k];
+      const int64_t row0 = ((int64_t)(ue % a.n_held) * a.B + ue / a.n_held) * a.R_total;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(a.o_part) + row0 * row_bytes);
+      for (int64_t i = threadIdx.x; i < a.R_total * row_bytes / 16; i += 1024) dst[i] = make_uint4(0, 0, 0, 0);
+      for (int i = threadIdx.x; i < a.R_total; i += 1024) a.lse_part[row0 + i] = -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) n_empty_s = 0;
     __syncthreads();
   }
   if (threadIdx.x == 0) tile_start[U] = carry;
@@ -1004,9 +1025,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------- fixup
-// Writes empty units (o = 0, lse = -inf) and merges the pieces of units cut by
-// range boundaries (the same LSE rule as the shard merge, base 2).  Blocks
-// per unit: up to 12, each taking chunks of 8 query rows; thread 0 builds the
+// Merges the pieces of units cut by range boundaries (the same LSE rule as the
+// shard merge, base 2).  Only range boundaries cut units, so block column k
+// serves boundary k (between ranges k and k + 1): the unit containing that
+// boundary's first tile, if the boundary falls inside it and no earlier boundary
+// does (the first boundary inside a unit merges all its pieces).  Blocks per
+// column: up to 12, each taking chunks of 8 query rows; thread 0 builds the
 // unit's piece list in shared memory, then one warp per row merges the pieces
 // with 16-byte loads and stores (lane l owns dims [16 l, 16 l + 16)).
 constexpr int kFixupThreads = 256;
@@ -1016,16 +1040,12 @@ constexpr int kFixupRows = kFixupThreads / 32;  // query rows per block: one per
 
 __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   __shared__ int32_t piece_s[kMaxPieces];
-  __shared__ int32_t npiece_s;
+  __shared__ int32_t npiece_s, unit_s;
   const int32_t U = a.B * a.n_held;
-  const int32_t u = blockIdx.x;
-  if (u >= U) return;
+  const int V = a.V;
+  const int64_t T = a.tile_start[U];
   const int row0 = blockIdx.y * kFixupRows + (threadIdx.x >> 5);  // this warp's first query row
   const int row_step = gridDim.y * kFixupRows;
-  const int b = u / a.n_held, rs = u % a.n_held;
-  const int64_t s = a.tile_start[u], e = a.tile_start[u + 1];
-  const int64_t T = a.tile_start[U];
-  const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total;
   const int lane = threadIdx.x & 31;
   auto store_row = [&](int64_t orow, const float (&v)[16]) {
     if (a.o_bf16) {
@@ -1046,17 +1066,27 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
       for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
   };
-  if (s == e) {
-    float z[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = 0.f;
-    for (int row = row0; row < a.R_total; row += row_step) {
-      store_row(out_row0 + row, z);
-      if (lane == 0) a.lse_part[out_row0 + row] = -INFINITY;
+  if (threadIdx.x == 0) {
+    const int k = blockIdx.x;
+    const int64_t x = range_lo(T, k + 1, V);  // the boundary's first tile
+    int unit = -1;
+    if (x > 0 && x < T) {
+      int32_t l = 0, h = U;  // the unit u with start[u] <= x < start[u + 1]
+      while (h - l > 1) {
+        const int32_t m = (l + h) >> 1;
+        if (a.tile_start[m] <= x) l = m; else h = m;
+      }
+      const int64_t su = a.tile_start[l];
+      if (su < x && (k == 0 || range_lo(T, k, V) <= su)) unit = l;
     }
-    return;
+    unit_s = unit;
   }
-  const int V = a.V;
+  __syncthreads();
+  const int32_t u = unit_s;
+  if (u < 0) return;
+  const int b = u / a.n_held, rs = u % a.n_held;
+  const int64_t s = a.tile_start[u], e = a.tile_start[u + 1];
+  const int64_t out_row0 = ((int64_t)rs * a.B + b) * a.R_total;
   if (threadIdx.x == 0) {
     auto part_of = [&](int64_t x) {  // range containing tile x
       int vv = (int)((x * V) / T);
@@ -1077,7 +1107,6 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   }
   __syncthreads();
   const int np = npiece_s;
-  if (np == 0) return;  // written whole by the main kernel
   for (int row = row0; row < a.R_total; row += row_step) {
     // Pieces two at a time: both pieces' lse and o loads are issued before
     // either is used (the row's loads are one latency, not one per piece).
@@ -1337,11 +1366,15 @@ int32_t launch_decode(const Plan& p, const dcp_layout_t* layout, int32_t shard_b
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
   partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, tkv4, a);
-  // one warp per row up to 96 rows; blocks loop over further row chunks (a large
-  // grid of blocks that mostly find their unit whole costs more than the loop)
-  const unsigned fix_y = (unsigned)std::min((a.R_total + kFixupRows - 1) / kFixupRows, 12);
-  fixup_kernel<<<dim3((unsigned)U, fix_y), kFixupThreads, 0, st>>>(a);
-  return launch_status(3);
+  // Cut units need their pieces merged: one block column per range boundary,
+  // one warp per row up to 96 rows, blocks looping over further row chunks.
+  // With one range per row group nothing is cut and no fixup runs.
+  if (p.V > 1) {
+    const unsigned fix_y = (unsigned)std::min((a.R_total + kFixupRows - 1) / kFixupRows, 12);
+    fixup_kernel<<<dim3((unsigned)(p.V - 1), fix_y), kFixupThreads, 0, st>>>(a);
+    return launch_status(3);
+  }
+  return launch_status(2);
 }
 
 }  // namespace
