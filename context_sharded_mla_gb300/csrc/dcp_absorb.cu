@@ -295,97 +295,115 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 // The LSE merge of the N partials and the output-side product in one kernel
 // ("MLA 的 Decode Context Parallelism", section 4, stage 7: the two-pass merge
 // and the w_vc up-projection at the head owner): per head h and 16 query
-// tokens, the merged latent output o[t, h, :] is formed in shared memory as a
-// bf16 operand and multiplied by w_vc[h] on the tensor core; only v (and the
-// merged lse) is written.  The merged o never reaches global memory.
-// The product is computed transposed, v^T = w_vc[h]^T o^T: A = w_vc[h] as an
-// MN-major [128 n][64 k] operand per K-step (straight from its [k][n] rows by
-// TMA), B = the merged rows as a K-major [16 tokens][64 k] operand, D = 128
-// TMEM lanes (output dims) x 16 columns (tokens).  So no operand rows are
-// padding, a CTA needs about 90 KB of shared memory (two per SM), and the
-// epilogue writes each token's 128 outputs as one coalesced row.
-//   warps 0-7   merge: row weights w_p = base^(lse_p - m) / Z (m = max_p lse_p),
-//               then every row's 512 dims as sum_p w_p o_p, rounded to bf16 into
-//               eight 128-byte-swizzled K-major tiles [16 rows][64 k]; warps
-//               0-3 then run the epilogue (warp w: output dims 32w .. 32w + 31)
-//   warp 8      TMA producer: w_vc[h] K-step by K-step, 4 stages
-//   warp 9      TMEM owner and MMA issuer: M=128, N=16, K=16 products
-// HBM-bound: the partials (N * 512 * 4 bytes per row in f32) are read once;
-// w_vc[h] (128 KB) is read once per 16 tokens, mostly from L2.
-constexpr int kMaThreads = 320;
+// tokens (a work item), the merged latent output o[t, h, :] is formed in
+// shared memory as a bf16 operand and multiplied by w_vc[h] on the tensor core;
+// only v (and the merged lse) is written.  The merged o never reaches global
+// memory.
+// Persistent: one CTA per SM walks the work items, its warps in five roles:
+//   producer (warp 12, one thread)  streams, K-step pair by K-step pair, each
+//        part's [16 tokens][128 dims] box of o_part by TMA into a ring of
+//        shared-memory stages (112 KB in flight), and w_vc[h]'s [64 k][128 n]
+//        K-steps into a ring of four;
+//   weights (warp 14)  the next item's row weights w_p = base^(lse_p - m) / Z
+//        and merged lse, into one of two weight buffers, while the current
+//        item is merged;
+//   merge (warps 4-11)  reduce the parts stage by stage (sum_p w_p o_p, from
+//        shared memory) and write each K-step's merged rows, rounded to bf16,
+//        as a 128-byte-swizzled K-major B tile [16 tokens][64 k];
+//   MMA (warp 13, one thread)  v^T = w_vc[h]^T o^T as soon as each tile is
+//        written: A = w_vc[h] (MN-major, M = 128 output dims), B = the merged
+//        tile (N = 16 tokens), K = 16 per product, into one of two TMEM
+//        accumulators;
+//   epilogue (warps 0-3)  TMEM lane = output dim, column = token: each token's
+//        128 outputs go out as one coalesced row.
+// Weights, B tiles and accumulators are double-buffered across items, so the
+// merge warps stream without waiting for either end of an item.  HBM-bound:
+// the partials (N * 512 * 4 bytes per row in f32) are read once; w_vc[h]
+// (128 KB) once per item, mostly from L2.
+constexpr int kMaThreads = 480;
+constexpr int kMaMergeWarp0 = 4;
 constexpr int kMaMergeWarps = 8;
-constexpr int kMaProducerWarp = 8;
-constexpr int kMaIssuerWarp = 9;
-constexpr int kMaTok = 16;                    // query tokens per CTA (the product's N)
+constexpr int kMaProducerWarp = 12;
+constexpr int kMaIssuerWarp = 13;
+constexpr int kMaWeightsWarp = 14;
+constexpr int kMaTok = 16;                    // query tokens per item (the product's N)
 constexpr int kMaKSteps = kDv / kKStep;       // 8
+constexpr int kMaBoxDims = 128;               // dims per o_part box (two K-steps)
 constexpr int kMaWStages = 4;
 constexpr int kMaMaxParts = 64;
+constexpr uint32_t kMaRingBytes = 112 * 1024;                                // o_part stages
 constexpr uint32_t kMaBTileBytes = kMaTok * 128;                             // [16 rows][64 k] bf16, 2 KB
 constexpr uint32_t kMaWStageBytes = 2 * kWBoxBytes;                          // [64 k][128 n] bf16, 16 KB
-constexpr uint32_t kMaW = 0;                                                 // 4 W stages, 64 KB
-constexpr uint32_t kMaB = kMaW + kMaWStages * kMaWStageBytes;                // 8 B tiles, 16 KB
-constexpr uint32_t kMaWts = kMaB + kMaKSteps * kMaBTileBytes;                // weights [parts][16] f32, 4 KB
-constexpr uint32_t kMaBars = kMaWts + kMaMaxParts * kMaTok * 4;              // full[4], empty[4], b_ready, done
-constexpr uint32_t kMaMisc = kMaBars + (2 * kMaWStages + 2) * 8;
+constexpr uint32_t kMaRing = 0;
+constexpr uint32_t kMaW = kMaRing + kMaRingBytes;                            // 4 W stages, 64 KB
+constexpr uint32_t kMaB = kMaW + kMaWStages * kMaWStageBytes;                // 2 x 8 B tiles, 32 KB
+constexpr uint32_t kMaWts = kMaB + 2 * kMaKSteps * kMaBTileBytes;            // weights [2][parts][16] f32, 8 KB
+constexpr int kMaMaxStages = kMaRingBytes / (kMaTok * kMaBoxDims * 2);       // 28 (bf16 boxes)
+// barriers: full[stages], empty[stages], w_full[4], w_empty[4], b_full[2][8], b_empty[2], d_full[2],
+// d_empty[2], g_full[2], g_empty[2] (the weight buffers)
+constexpr int kMaNumBars = 2 * kMaMaxStages + 2 * kMaWStages + 2 * kMaKSteps + 10;
+constexpr uint32_t kMaBars = kMaWts + 2 * kMaMaxParts * kMaTok * 4;
+constexpr uint32_t kMaMisc = kMaBars + kMaNumBars * 8;
 constexpr uint32_t kMaBytes = kMaMisc + 16 + 1024;                            // + alignment slack
 
 struct MergeAbsorbArgs {
   int64_t T;
   int32_t H, n_parts, base2;
-  const void* o_part;     // [n_parts, T, H, 512] f32 or bf16
-  const float* lse_part;  // [n_parts, T, H]
-  void* v;                // [T, H, 128] f32 or bf16
+  int32_t n_tiles, n_items;   // token tiles of 16, items = H * n_tiles
+  const float* lse_part;      // [n_parts, T, H]
+  void* v;                    // [T, H, 128] f32 or bf16
   int32_t v_bf16;
-  float* lse;             // [T, H] or null
+  float* lse;                 // [T, H] or null
   int32_t* status;
 };
 
-template <int kInBf16>
-__device__ __forceinline__ float4 load_part4(const void* base, int64_t elem) {
-  if (kInBf16) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem));
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-  }
-  return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem));
-}
-
 template <int kInBf16, int kBase2>
-__global__ void __launch_bounds__(kMaThreads, 2)
-    merge_absorb_kernel(const __grid_constant__ CUtensorMap tmap_w, MergeAbsorbArgs a) {
+__global__ void __launch_bounds__(kMaThreads, 1)
+    merge_absorb_kernel(const __grid_constant__ CUtensorMap tmap_o, const __grid_constant__ CUtensorMap tmap_w,
+                        MergeAbsorbArgs a) {
+  constexpr uint32_t kBoxBytes = kMaTok * kMaBoxDims * (kInBf16 ? 2 : 4);
+  constexpr int kStages = kMaRingBytes / kBoxBytes;   // 14 (f32) or 28 (bf16)
+  constexpr int kPairs = kMaKSteps / 2;               // boxes per part and item
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* wts = reinterpret_cast<float*>(smem + kMaWts);
+  float* wts = reinterpret_cast<float*>(smem + kMaWts);  // [2][kMaMaxParts][16]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMaBars);
-  uint64_t* empty = full + kMaWStages;
-  uint64_t* b_ready = empty + kMaWStages;
-  uint64_t* done = b_ready + 1;
+  uint64_t* empty = full + kStages;
+  uint64_t* w_full = empty + kStages;
+  uint64_t* w_empty = w_full + kMaWStages;
+  uint64_t* b_full = w_empty + kMaWStages;            // [2][8]
+  uint64_t* b_empty = b_full + 2 * kMaKSteps;         // [2]
+  uint64_t* d_full = b_empty + 2;                     // [2]
+  uint64_t* d_empty = d_full + 2;                     // [2]
+  uint64_t* g_full = d_empty + 2;                     // [2] weights ready
+  uint64_t* g_empty = g_full + 2;                     // [2] weights no longer read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMaMisc);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kMaMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x;
-  const int64_t t0 = (int64_t)blockIdx.y * kMaTok;
+  const int n = a.n_parts;
 
-  auto issue_w = [&](int ks) {
-    const int s = ks % kMaWStages;
-    uint8_t* st = smem + kMaW + s * kMaWStageBytes;
-    mbar_arrive_expect_tx(&full[s], kMaWStageBytes);
-    tma_load_3d(st, &tmap_w, &full[s], 0, ks * kKStep, h);
-    tma_load_3d(st + kWBoxBytes, &tmap_w, &full[s], 64, ks * kKStep, h);
-  };
   if (warp == kMaProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_o);
     prefetch_tmap(&tmap_w);
-    for (int s = 0; s < kMaWStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMaMergeWarps);
     }
-    mbar_init(b_ready, kMaMergeWarps);
-    mbar_init(done, 1);
+    for (int i = 0; i < kMaWStages; ++i) {
+      mbar_init(&w_full[i], 1);
+      mbar_init(&w_empty[i], 1);
+    }
+    for (int i = 0; i < 2 * kMaKSteps; ++i) mbar_init(&b_full[i], kMaMergeWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b_empty[i], 1);
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], 4);
+      mbar_init(&g_full[i], 1);
+      mbar_init(&g_empty[i], kMaMergeWarps);
+    }
     *abort_s = 0;
     fence_barrier_init();
-    for (int ks = 0; ks < kMaWStages; ++ks) issue_w(ks);  // w_vc[h] starts streaming at once
   }
   if (warp == kMaIssuerWarp) {
     tmem_alloc(tmem_slot, 32);
@@ -399,120 +417,185 @@ __global__ void __launch_bounds__(kMaThreads, 2)
   if (warp == kMaProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int ks = kMaWStages; ks < kMaKSteps; ++ks) {
-        if (!mbar_wait(&empty[ks % kMaWStages], ((ks / kMaWStages) - 1) & 1, abort_s)) break;
-        issue_w(ks);
+      uint32_t q = 0, wq = 0;  // o_part boxes and w_vc K-steps issued so far
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        const int h = item / a.n_tiles;
+        const int64_t t0 = (int64_t)(item % a.n_tiles) * kMaTok;
+        for (int kp = 0; kp < kPairs && ok; ++kp) {
+          for (int j = 0; j < 2; ++j, ++wq) {  // w_vc[h], K-steps 2 kp and 2 kp + 1
+            const uint32_t ws = wq % kMaWStages;
+            if (!mbar_wait(&w_empty[ws], ((wq / kMaWStages) & 1) ^ 1, abort_s)) { ok = false; break; }
+            uint8_t* st = smem + kMaW + ws * kMaWStageBytes;
+            mbar_arrive_expect_tx(&w_full[ws], kMaWStageBytes);
+            tma_load_3d(st, &tmap_w, &w_full[ws], 0, (2 * kp + j) * kKStep, h);
+            tma_load_3d(st + kWBoxBytes, &tmap_w, &w_full[ws], 64, (2 * kp + j) * kKStep, h);
+          }
+          for (int p = 0; p < n && ok; ++p, ++q) {  // every part's [16 tokens][128 dims] box
+            const uint32_t qs = q % kStages;
+            if (!mbar_wait(&empty[qs], ((q / kStages) & 1) ^ 1, abort_s)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[qs], kBoxBytes);
+            tma_load_3d(smem + kMaRing + qs * kBoxBytes, &tmap_o, &full[qs], kp * kMaBoxDims, h,
+                        (int32_t)((int64_t)p * a.T + t0));
+          }
+        }
       }
     }
   } else if (warp == kMaIssuerWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kMaTok, 1, 0);  // A = w_vc MN-major, B = o K-major
-      bool ok = mbar_wait(b_ready, 0, abort_s);
-      for (int ks = 0; ks < kMaKSteps && ok; ++ks) {
-        const int s = ks % kMaWStages;
-        if (!mbar_wait(&full[s], (ks / kMaWStages) & 1, abort_s)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t wdesc = sw128_desc(smem_u32(smem + kMaW + s * kMaWStageBytes), kWBoxBytes, 1024);
-        const uint64_t bdesc = sw128_desc(smem_u32(smem + kMaB + ks * kMaBTileBytes), 16, 1024);
+      uint32_t wq = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++it) {
+        const uint32_t buf = it & 1, use = (it >> 1) & 1;
+        for (int ks = 0; ks < kMaKSteps && ok; ++ks, ++wq) {
+          const uint32_t ws = wq % kMaWStages;
+          if (!mbar_wait(&b_full[buf * kMaKSteps + ks], use, abort_s) ||
+              !mbar_wait(&w_full[ws], (wq / kMaWStages) & 1, abort_s) ||
+              (ks == 0 && !mbar_wait(&d_empty[buf], use ^ 1, abort_s))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t wdesc = sw128_desc(smem_u32(smem + kMaW + ws * kMaWStageBytes), kWBoxBytes, 1024);
+          const uint64_t bdesc =
+              sw128_desc(smem_u32(smem + kMaB + (buf * kMaKSteps + ks) * kMaBTileBytes), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kKStep / 16; ++kk)
-          mma_bf16_ss(tmem, wdesc + kk * (2048 >> 4), bdesc + kk * (32 >> 4), idesc, (ks | kk) != 0);
-        mma_commit(&empty[s]);
+          for (int kk = 0; kk < kKStep / 16; ++kk)
+            mma_bf16_ss(tmem + 16 * buf, wdesc + kk * (2048 >> 4), bdesc + kk * (32 >> 4), idesc, (ks | kk) != 0);
+          mma_commit(&w_empty[ws]);
+        }
+        if (ok) {
+          mma_commit(&d_full[buf]);
+          mma_commit(&b_empty[buf]);
+        }
       }
-      if (ok) mma_commit(done);
+    }
+  } else if (warp == kMaWeightsWarp) {
+    // ------------------------------------------------------------------ row weights, one item ahead
+    // lanes 0-15 serve the item's 16 tokens; every part's lse is loaded at once
+    const int64_t rows = a.T * a.H;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++it) {
+      const int h = item / a.n_tiles;
+      const int64_t t = (int64_t)(item % a.n_tiles) * kMaTok + (lane & 15);
+      const uint32_t buf = it & 1, use = (it >> 1) & 1;
+      if (!warp_wait_all(&g_empty[buf], use ^ 1, abort_s)) { ok = false; break; }
+      float* w = wts + buf * kMaMaxParts * kMaTok;
+      if (lane < kMaTok) {
+        const bool live = t < a.T;
+        float m = -INFINITY;
+        for (int p = 0; p < n; ++p) {
+          const float l = live ? __ldg(a.lse_part + p * rows + t * a.H + h) : -INFINITY;
+          w[p * kMaTok + lane] = l;
+          m = fmaxf(m, l);
+        }
+        float z = 0.f;
+        for (int p = 0; p < n; ++p) {
+          const float l = w[p * kMaTok + lane];
+          const float e = (m == -INFINITY || l == -INFINITY) ? 0.f : (kBase2 ? exp2f(l - m) : expf(l - m));
+          w[p * kMaTok + lane] = e;
+          z += e;
+        }
+        const float inv = z > 0.f ? 1.f / z : 0.f;
+        for (int p = 0; p < n; ++p) w[p * kMaTok + lane] *= inv;
+        if (live && a.lse) a.lse[t * a.H + h] = z > 0.f ? m + (kBase2 ? log2f(z) : logf(z)) : -INFINITY;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&g_full[buf]);
+    }
+  } else if (warp >= kMaMergeWarp0) {
+    // ------------------------------------------------------------------ merge warps 4-11
+    const int mt = tid - 32 * kMaMergeWarp0;  // 0 .. 255
+    const int r = mt >> 4;                    // this thread's token within the item
+    const int c4 = mt & 15;                   // its 4-dim group within each 64-dim K-step
+    uint32_t q = 0, it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x, ++it) {
+      const uint32_t buf = it & 1, use = (it >> 1) & 1;
+      // the item's weights, and this buffer's B tiles free (products of two items ago done)
+      if (!warp_wait_all(&g_full[buf], use, abort_s) || !warp_wait_all(&b_empty[buf], use ^ 1, abort_s)) {
+        ok = false;
+        break;
+      }
+      const float* w = wts + buf * kMaMaxParts * kMaTok;
+      for (int kp = 0; kp < kPairs && ok; ++kp) {
+        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+        for (int p = 0; p < n; ++p, ++q) {
+          const uint32_t qs = q % kStages;
+          if (!warp_wait_all(&full[qs], (q / kStages) & 1, abort_s)) { ok = false; break; }
+          const float wp = w[p * kMaTok + r];
+          const uint8_t* box = smem + kMaRing + qs * kBoxBytes;
+          float4 x0, x1;
+          if (kInBf16) {
+            const uint2 u0 = *reinterpret_cast<const uint2*>(box + r * kMaBoxDims * 2 + c4 * 8);
+            const uint2 u1 = *reinterpret_cast<const uint2*>(box + r * kMaBoxDims * 2 + 128 + c4 * 8);
+            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u0.x));
+            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u0.y));
+            const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u1.x));
+            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u1.y));
+            x0 = make_float4(a0.x, a0.y, b0.x, b0.y);
+            x1 = make_float4(a1.x, a1.y, b1.x, b1.y);
+          } else {
+            x0 = *reinterpret_cast<const float4*>(box + r * kMaBoxDims * 4 + c4 * 16);
+            x1 = *reinterpret_cast<const float4*>(box + r * kMaBoxDims * 4 + 256 + c4 * 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[qs]);
+          acc0.x = fmaf(wp, x0.x, acc0.x); acc0.y = fmaf(wp, x0.y, acc0.y);
+          acc0.z = fmaf(wp, x0.z, acc0.z); acc0.w = fmaf(wp, x0.w, acc0.w);
+          acc1.x = fmaf(wp, x1.x, acc1.x); acc1.y = fmaf(wp, x1.y, acc1.y);
+          acc1.z = fmaf(wp, x1.z, acc1.z); acc1.w = fmaf(wp, x1.w, acc1.w);
+        }
+        if (!ok) break;
+        // K-steps 2 kp and 2 kp + 1 of the merged rows -> bf16, swizzled K-major:
+        // 16-byte chunk c16 of row r at r * 128 + ((c16 ^ (r % 8)) * 16)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float4 y = j ? acc1 : acc0;
+          const uint32_t off = kMaB + (buf * kMaKSteps + 2 * kp + j) * kMaBTileBytes + r * 128 +
+                               ((((c4 >> 1) ^ (r & 7))) << 4) + (c4 & 1) * 8;
+          st_shared_v2(smem_u32(smem) + off, pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&b_full[buf * kMaKSteps + 2 * kp]);
+          mbar_arrive(&b_full[buf * kMaKSteps + 2 * kp + 1]);
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&g_empty[buf]);  // this item's weights are no longer read
     }
   } else {
-    // ------------------------------------------------------------------ merge warps 0-7, then the epilogue
-    constexpr int kMergeThreads = 32 * kMaMergeWarps;
-    // row weights: all parts' lse of the 16 tokens land in shared memory at once
-    // (one load per thread), then thread r < 16 of warp 0 turns token t0 + r's
-    // into weights
-    const int64_t rows = a.T * a.H;
-    for (int i = tid; i < a.n_parts * kMaTok; i += kMergeThreads) {
-      const int p = i / kMaTok, r = i % kMaTok;
-      const int64_t t = t0 + r;
-      wts[i] = t < a.T ? __ldg(a.lse_part + p * rows + t * a.H + h) : -INFINITY;
-    }
-    named_bar_sync(1, kMergeThreads);
-    if (warp == 0 && lane < kMaTok) {
-      const int64_t t = t0 + lane;
-      float m = -INFINITY;
-      for (int p = 0; p < a.n_parts; ++p) m = fmaxf(m, wts[p * kMaTok + lane]);
-      float z = 0.f;
-      for (int p = 0; p < a.n_parts; ++p) {
-        const float l = wts[p * kMaTok + lane];
-        const float w = (m == -INFINITY || l == -INFINITY) ? 0.f : (kBase2 ? exp2f(l - m) : expf(l - m));
-        wts[p * kMaTok + lane] = w;
-        z += w;
-      }
-      const float inv = z > 0.f ? 1.f / z : 0.f;
-      for (int p = 0; p < a.n_parts; ++p) wts[p * kMaTok + lane] *= inv;
-      if (t < a.T && a.lse) a.lse[t * a.H + h] = z > 0.f ? m + (kBase2 ? log2f(z) : logf(z)) : -INFINITY;
-    }
-    named_bar_sync(1, kMergeThreads);
-    // merged rows: float4 f = tid + 256 i (i < 8) is row f / 128, dims 4 (f % 128) .. + 4
-    {
-      constexpr int kPer = kMaTok * (kDv / 4) / kMergeThreads;  // 8
-      float4 acc[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-      for (int p = 0; p < a.n_parts; ++p) {
-        float4 x[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int f = tid + kMergeThreads * i, r = f >> 7, c = f & 127;
-          const int64_t t = t0 + r;
-          x[i] = (t < a.T && wts[p * kMaTok + r] != 0.f)
-                     ? load_part4<kInBf16>(a.o_part, ((int64_t)p * rows + t * a.H + h) * kDv + 4 * c)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int f = tid + kMergeThreads * i, r = f >> 7;
-          const float w = wts[p * kMaTok + r];
-          acc[i].x = fmaf(w, x[i].x, acc[i].x);
-          acc[i].y = fmaf(w, x[i].y, acc[i].y);
-          acc[i].z = fmaf(w, x[i].z, acc[i].z);
-          acc[i].w = fmaf(w, x[i].w, acc[i].w);
-        }
-      }
-      // bf16 into the swizzled K-major tiles: 16-byte chunk c16 of row r sits at
-      // r * 128 + ((c16 ^ (r % 8)) * 16) of K-step tile c / 16
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int f = tid + kMergeThreads * i, r = f >> 7, c = f & 127;
-        const int ks = c >> 4, c4 = c & 15;
-        const uint32_t off = kMaB + ks * kMaBTileBytes + r * 128 + (((c4 >> 1) ^ (r & 7)) << 4) + (c4 & 1) * 8;
-        st_shared_v2(smem_u32(smem) + off, pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
-      }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b_ready);
-    if (warp < 4) {
-      // epilogue: TMEM lane 32w + l holds output dim 32w + l for the 16 tokens
-      // (columns).  The TMEM load is warp-collective (.sync.aligned): every lane
-      // of the warp runs it; only the stores depend on the token being live.
-      const bool ok = warp_wait_all(done, 0, abort_s);  // warp-uniform
+    // ------------------------------------------------------------------ epilogue warps 0-3
+    // TMEM lane 32w + l holds output dim 32w + l for the item's 16 tokens
+    // (columns).  The TMEM load is warp-collective (.sync.aligned): every lane
+    // runs it; only the stores depend on the token being live.
+    uint32_t it = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++it) {
+      const int h = item / a.n_tiles;
+      const int64_t t0 = (int64_t)(item % a.n_tiles) * kMaTok;
+      const uint32_t buf = it & 1, use = (it >> 1) & 1;
+      if (!warp_wait_all(&d_full[buf], use, abort_s)) break;
       tc_fence_after();
-      if (ok) {
-        uint32_t r[16];
-        tmem_ld32x16_sync(tmem + ((uint32_t)(32 * warp) << 16), r);
-        const int n = 32 * warp + lane;
+      uint32_t rv[16];
+      tmem_ld32x16_sync(tmem + ((uint32_t)(32 * warp) << 16) + 16 * buf, rv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[buf]);
+      const int nd = 32 * warp + lane;
 #pragma unroll
-        for (int j = 0; j < kMaTok; ++j) {
-          const int64_t t = t0 + j;
-          if (t >= a.T) break;
-          if (a.v_bf16)
-            static_cast<__nv_bfloat16*>(a.v)[(t * a.H + h) * 128 + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
-          else
-            static_cast<float*>(a.v)[(t * a.H + h) * 128 + n] = __uint_as_float(r[j]);
-        }
+      for (int j = 0; j < kMaTok; ++j) {
+        const int64_t t = t0 + j;
+        if (t >= a.T) break;
+        if (a.v_bf16)
+          static_cast<__nv_bfloat16*>(a.v)[(t * a.H + h) * 128 + nd] = __float2bfloat16_rn(__uint_as_float(rv[j]));
+        else
+          static_cast<float*>(a.v)[(t * a.H + h) * 128 + nd] = __uint_as_float(rv[j]);
       }
     }
   }
@@ -625,13 +708,32 @@ extern "C" int32_t dcp_absorb_o(int64_t T, int32_t H, const void* o, int32_t o_d
 namespace {
 
 template <int kInBf16, int kBase2>
-int32_t launch_merge_absorb(const CUtensorMap& tw, const MergeAbsorbArgs& a, cudaStream_t st) {
+int32_t launch_merge_absorb(const CUtensorMap& to, const CUtensorMap& tw, const MergeAbsorbArgs& a, cudaStream_t st) {
   static SmemLimit limit;
   if (!limit.ensure(reinterpret_cast<const void*>(&merge_absorb_kernel<kInBf16, kBase2>), kMaBytes))
     return DCP_ERR_CUDA;
-  const dim3 grid((unsigned)a.H, (unsigned)((a.T + kMaTok - 1) / kMaTok));
-  merge_absorb_kernel<kInBf16, kBase2><<<grid, kMaThreads, kMaBytes, st>>>(tw, a);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    return DCP_ERR_CUDA;
+  const int grid = a.n_items < sms ? a.n_items : sms;  // persistent: one CTA per SM
+  merge_absorb_kernel<kInBf16, kBase2><<<grid, kMaThreads, kMaBytes, st>>>(to, tw, a);
   return launch_status();
+}
+
+// o_part [n_parts, T, H, 512] seen as (dims, head, part-major token row):
+// boxes of [16 rows][1 head][128 dims], no swizzle.
+bool make_tmap_parts(CUtensorMap* m, const void* base, int n_parts, int64_t T, int64_t H, bool bf16) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  const uint64_t e = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {(cuuint64_t)kDv, (cuuint64_t)H, (cuuint64_t)(n_parts * T)};
+  cuuint64_t strides[2] = {(cuuint64_t)kDv * e, (cuuint64_t)(H * kDv * e)};
+  cuuint32_t box[3] = {(cuuint32_t)kMaBoxDims, 1, (cuuint32_t)kMaTok};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -640,29 +742,31 @@ extern "C" int32_t dcp_lse_merge_absorb_o(int32_t n_parts, int64_t T, int32_t H,
                                           int32_t o_part_dtype, const float* lse_part, int32_t lse_base,
                                           const void* w_vc, void* v, int32_t v_dtype, float* lse, int32_t* status,
                                           void* stream) {
-  if (n_parts < 1 || n_parts > kMaMaxParts || T < 0 || H < 1 || H > 65535 || (T + kMaTok - 1) / kMaTok > 65535)
-    return DCP_ERR_INVALID;
+  if (n_parts < 1 || n_parts > kMaMaxParts || T < 0 || H < 1 || H > 65535) return DCP_ERR_INVALID;
   if ((o_part_dtype != DCP_F32 && o_part_dtype != DCP_BF16) || (v_dtype != DCP_F32 && v_dtype != DCP_BF16))
     return DCP_ERR_INVALID;
   if (lse_base != DCP_LSE_BASE_E && lse_base != DCP_LSE_BASE_2) return DCP_ERR_INVALID;
   if (T == 0) return DCP_OK;
   if (!o_part || !lse_part || !w_vc || !v) return DCP_ERR_INVALID;
   if (!aligned16(o_part) || !aligned16(w_vc) || !aligned16(v)) return DCP_ERR_INVALID;
-  CUtensorMap tw;
-  if (!make_tmap_w(&tw, w_vc, H, kDv, 128)) return DCP_ERR_CUDA;
+  const int64_t n_tiles = (T + kMaTok - 1) / kMaTok;
+  if (n_tiles * H > INT32_MAX || (int64_t)n_parts * T > INT32_MAX) return DCP_ERR_UNSUPPORTED;
+  const bool ib = o_part_dtype == DCP_BF16;
+  CUtensorMap to, tw;
+  if (!make_tmap_parts(&to, o_part, n_parts, T, H, ib) || !make_tmap_w(&tw, w_vc, H, kDv, 128)) return DCP_ERR_CUDA;
   MergeAbsorbArgs a{};
   a.T = T;
   a.H = H;
   a.n_parts = n_parts;
   a.base2 = lse_base == DCP_LSE_BASE_2;
-  a.o_part = o_part;
+  a.n_tiles = (int32_t)n_tiles;
+  a.n_items = (int32_t)(n_tiles * H);
   a.lse_part = lse_part;
   a.v = v;
   a.v_bf16 = v_dtype == DCP_BF16;
   a.lse = lse;
   a.status = status;
   cudaStream_t st = as_stream(stream);
-  const bool ib = o_part_dtype == DCP_BF16;
-  if (ib) return a.base2 ? launch_merge_absorb<1, 1>(tw, a, st) : launch_merge_absorb<1, 0>(tw, a, st);
-  return a.base2 ? launch_merge_absorb<0, 1>(tw, a, st) : launch_merge_absorb<0, 0>(tw, a, st);
+  if (ib) return a.base2 ? launch_merge_absorb<1, 1>(to, tw, a, st) : launch_merge_absorb<1, 0>(to, tw, a, st);
+  return a.base2 ? launch_merge_absorb<0, 1>(to, tw, a, st) : launch_merge_absorb<0, 0>(to, tw, a, st);
 }
