@@ -346,7 +346,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 latent rows and queries, shuffled block table)",
-        "config": config_dict(cfg, st, world),
+        "config": config_dict(cfg, st["S"], world, args.exchange if group else None),
         "roofline": roof,
         "partial_ms": round(part_ms_avg, 5),
         "step_ms_median": round(statistics.median(step_ms), 5),
@@ -459,10 +459,7 @@ def run_relayout_op(args, cfg, rank, world, dist, device):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 latent rows, shuffled source and destination page tables)",
-        "config": {"workload": f"relayout of {workloads.DESCRIPTIONS.get(cfg.name, cfg.name)} requests, prefilled "
-                               f"without context sharding (source pages of {Ps} rows), into all {cfg.N} shards",
-                   "B": cfg.B, "tokens": T, "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P,
-                   "source_page_size": Ps, "l2": "source and destination far larger than L2, no flush"},
+        "config": relayout_config(cfg),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
                      "kernel": "kv_relayout_kernel (CUDA events on the launching stream)",
@@ -626,11 +623,7 @@ def run_absorb_op(args, cfg, rank, world, dist, device):
         "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) query projection and o; weights N(0, 1/fan_in), bf16)",
-        "config": {"workload": f"absorption products at the decode shapes of "
-                               f"{workloads.DESCRIPTIONS.get(cfg.name, cfg.name)}: T={T} query tokens, H={H}, "
-                               f"w_kc [H,128,512], w_vc [H,512,128], o {str(o_dtype).split('.')[-1]}, v bf16",
-                   "T": T, "H": H, "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB written and "
-                                          "read back, outside the timed kernels)"},
+        "config": absorb_config(cfg),
         "kernels_us": {"absorb_q": round(q_ms * 1e3, 3), "absorb_o": round(o_ms * 1e3, 3),
                        "lse_merge": round(merge_ms * 1e3, 3),
                        "lse_merge_absorb_o": round(statistics.mean(fused) * 1e3, 3)},
@@ -755,18 +748,37 @@ def recorded_traffic(key):
         return None
 
 
-def config_dict(cfg, st, world):
-    S = st["S"]
+def config_dict(cfg, S, world, strategy=None):
+    """The decode step's `config`, from the workload alone (both arms print the same one)."""
     d = {"workload": workloads.DESCRIPTIONS[cfg.name] if cfg.name in workloads.DESCRIPTIONS else cfg.name,
          "B": cfg.B, "H": cfg.H, "q_len": cfg.q_len, "S_total": int(S.sum()), "S_max": int(S.max()),
          "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P, "lse_base": "2" if cfg.base == 2 else "e",
          "new_tokens_per_request": max(cfg.append, cfg.chunk), "out_dtype": cfg.out_dtype,
          "partials": "fp32", "global_batch": cfg.B, "seq_len": int(S.max()),
-         "parallelism": ("1 GPU holds all N shards" if not hasattr(st["dec"], "xchg") else
+         "parallelism": ("1 GPU holds all N shards" if strategy is None else
                          f"DCP over {world} GPUs: {cfg.N // world} shards and {cfg.H // world} output heads per GPU, "
-                         f"query replicated, {getattr(st['dec'].xchg, 'strategy', '')} exchange of the partials"),
+                         f"query replicated, {strategy} exchange of the partials"),
          "l2": f"inputs larger than L2 ({int(S.sum()) * KV_ROW_BYTES / 1e9:.2f} GB of KV per step), no flush"}
     return d
+
+
+def relayout_config(cfg):
+    S = workloads.lengths(cfg)
+    Ps = RELAYOUT_SRC_PAGE
+    return {"workload": f"relayout of {workloads.DESCRIPTIONS.get(cfg.name, cfg.name)} requests, prefilled "
+                        f"without context sharding (source pages of {Ps} rows), into all {cfg.N} shards",
+            "B": cfg.B, "tokens": int(S.sum()), "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P,
+            "source_page_size": Ps, "l2": "source and destination far larger than L2, no flush"}
+
+
+def absorb_config(cfg):
+    T, H = cfg.B * cfg.q_len, cfg.H
+    o_dtype = "float32" if cfg.out_dtype == "f32" else "bfloat16"
+    return {"workload": f"absorption products at the decode shapes of "
+                        f"{workloads.DESCRIPTIONS.get(cfg.name, cfg.name)}: T={T} query tokens, H={H}, "
+                        f"w_kc [H,128,512], w_vc [H,512,128], o {o_dtype}, v bf16",
+            "T": T, "H": H, "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB written and "
+                                   "read back, outside the timed kernels)"}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
@@ -852,9 +864,9 @@ def run_reference(args, cfg, rank, world):
     return {
         "metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": workloads.DESCRIPTIONS.get(cfg.name, cfg.name),
-                                                  "B": cfg.B, "H": cfg.H, "n_shards": cfg.N},
+        "higher_is_better": True, "scaling": "strong" if world > 1 or args.group else "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": config_dict(cfg, workloads.lengths(cfg), world, args.exchange if world > 1 or args.group else None),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -879,8 +891,8 @@ def run_reference_op(args, cfg, rank, world):
         "metric": metric, "impl": "reference", "value": round(value, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": workloads.DESCRIPTIONS.get(cfg.name, cfg.name),
-                                                  "op": args.op},
+        "data": "synthetic (seeded)",
+        "config": relayout_config(cfg) if args.op == "relayout" else absorb_config(cfg),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"per step: {desc}"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -936,7 +948,7 @@ def main(argv=None):
         run_op, time_op = ((run_relayout_op, time_oracle_relayout) if args.op == "relayout"
                            else (run_absorb_op, time_oracle_absorb))
         result = run_op(args, cfg, rank, world, dist, device)
-        if rank == 0 and not args.no_cpu_baseline:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
             nbytes, secs, desc = time_op(cfg, args.cpu_budget)
             result["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": 1,
                                       "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
@@ -946,7 +958,7 @@ def main(argv=None):
             dist.destroy_process_group()
         return 0
     result = run_ours(args, cfg, rank, world, dist, device)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         kv_bytes, secs, desc = time_oracle(cfg, args.cpu_budget, device=device)
         result["cpu_baseline"] = {"value": round(kv_bytes / secs / 1e9, 6), "unit": "GB/s",
                                   "cores": oracle_threads(), "kind": "oracle", "sample": desc,
