@@ -299,11 +299,12 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 // shared memory as a bf16 operand and multiplied by w_vc[h] on the tensor core;
 // only v (and the merged lse) is written.  The merged o never reaches global
 // memory.
-// Persistent: one CTA per SM walks the work items, its warps in five roles:
-//   producer (warp 12, one thread)  streams, K-step pair by K-step pair, each
-//        part's [16 tokens][128 dims] box of o_part by TMA into a ring of
-//        shared-memory stages (112 KB in flight), and w_vc[h]'s [64 k][128 n]
-//        K-steps into a ring of four;
+// Persistent: one CTA per SM walks the work items, its warps in six roles:
+//   producers (warps 12 and 15, one thread each)  stream, two K-steps at a
+//        time, each part's [16 tokens][128 dims] box of o_part by TMA into a
+//        ring of shared-memory stages (144 KB in flight), and, on their own,
+//        w_vc[h]'s [64 k][128 n] K-steps into a ring of two, so that neither
+//        stream waits for the other's ring;
 //   weights (warp 14)  the next item's row weights w_p = base^(lse_p - m) / Z
 //        and merged lse, into one of two weight buffers, while the current
 //        item is merged;
@@ -320,26 +321,29 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 // merge warps stream without waiting for either end of an item.  HBM-bound:
 // the partials (N * 512 * 4 bytes per row in f32) are read once; w_vc[h]
 // (128 KB) once per item, mostly from L2.
-constexpr int kMaThreads = 480;
+constexpr int kMaThreads = 512;
 constexpr int kMaMergeWarp0 = 4;
 constexpr int kMaMergeWarps = 8;
 constexpr int kMaProducerWarp = 12;
 constexpr int kMaIssuerWarp = 13;
 constexpr int kMaWeightsWarp = 14;
+constexpr int kMaWProducerWarp = 15;
 constexpr int kMaTok = 16;                    // query tokens per item (the product's N)
 constexpr int kMaKSteps = kDv / kKStep;       // 8
-constexpr int kMaBoxDims = 128;               // dims per o_part box (two K-steps)
-constexpr int kMaWStages = 4;
+constexpr int kMaBoxDims = 128;               // dims per o_part box (two K-steps; 256-dim boxes, half as
+                                              // many stages, measured slower)
+constexpr int kMaKPerBox = kMaBoxDims / kKStep;
+constexpr int kMaWStages = 2;
 constexpr int kMaMaxParts = 64;
-constexpr uint32_t kMaRingBytes = 112 * 1024;                                // o_part stages
+constexpr uint32_t kMaRingBytes = 144 * 1024;                                // o_part stages
 constexpr uint32_t kMaBTileBytes = kMaTok * 128;                             // [16 rows][64 k] bf16, 2 KB
 constexpr uint32_t kMaWStageBytes = 2 * kWBoxBytes;                          // [64 k][128 n] bf16, 16 KB
 constexpr uint32_t kMaRing = 0;
-constexpr uint32_t kMaW = kMaRing + kMaRingBytes;                            // 4 W stages, 64 KB
+constexpr uint32_t kMaW = kMaRing + kMaRingBytes;                            // 2 W stages, 32 KB
 constexpr uint32_t kMaB = kMaW + kMaWStages * kMaWStageBytes;                // 2 x 8 B tiles, 32 KB
 constexpr uint32_t kMaWts = kMaB + 2 * kMaKSteps * kMaBTileBytes;            // weights [2][parts][16] f32, 8 KB
-constexpr int kMaMaxStages = kMaRingBytes / (kMaTok * kMaBoxDims * 2);       // 28 (bf16 boxes)
-// barriers: full[stages], empty[stages], w_full[4], w_empty[4], b_full[2][8], b_empty[2], d_full[2],
+constexpr int kMaMaxStages = kMaRingBytes / (kMaTok * kMaBoxDims * 2);       // 36 (bf16 boxes)
+// barriers: full[stages], empty[stages], w_full[2], w_empty[2], b_full[2][8], b_empty[2], d_full[2],
 // d_empty[2], g_full[2], g_empty[2] (the weight buffers)
 constexpr int kMaNumBars = 2 * kMaMaxStages + 2 * kMaWStages + 2 * kMaKSteps + 10;
 constexpr uint32_t kMaBars = kMaWts + 2 * kMaMaxParts * kMaTok * 4;
@@ -362,8 +366,8 @@ __global__ void __launch_bounds__(kMaThreads, 1)
     merge_absorb_kernel(const __grid_constant__ CUtensorMap tmap_o, const __grid_constant__ CUtensorMap tmap_w,
                         MergeAbsorbArgs a) {
   constexpr uint32_t kBoxBytes = kMaTok * kMaBoxDims * (kInBf16 ? 2 : 4);
-  constexpr int kStages = kMaRingBytes / kBoxBytes;   // 14 (f32) or 28 (bf16)
-  constexpr int kPairs = kMaKSteps / 2;               // boxes per part and item
+  constexpr int kStages = kMaRingBytes / kBoxBytes;   // 18 (f32) or 36 (bf16)
+  constexpr int kBoxesPerPart = kMaKSteps / kMaKPerBox;   // boxes per part and item
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* wts = reinterpret_cast<float*>(smem + kMaWts);  // [2][kMaMaxParts][16]
@@ -415,29 +419,38 @@ __global__ void __launch_bounds__(kMaThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kMaProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer: o_part boxes
     if (lane == 0) {
-      uint32_t q = 0, wq = 0;  // o_part boxes and w_vc K-steps issued so far
+      uint32_t q = 0;  // o_part boxes issued so far
       bool ok = true;
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
         const int h = item / a.n_tiles;
         const int64_t t0 = (int64_t)(item % a.n_tiles) * kMaTok;
-        for (int kp = 0; kp < kPairs && ok; ++kp) {
-          for (int j = 0; j < 2; ++j, ++wq) {  // w_vc[h], K-steps 2 kp and 2 kp + 1
-            const uint32_t ws = wq % kMaWStages;
-            if (!mbar_wait(&w_empty[ws], ((wq / kMaWStages) & 1) ^ 1, abort_s)) { ok = false; break; }
-            uint8_t* st = smem + kMaW + ws * kMaWStageBytes;
-            mbar_arrive_expect_tx(&w_full[ws], kMaWStageBytes);
-            tma_load_3d(st, &tmap_w, &w_full[ws], 0, (2 * kp + j) * kKStep, h);
-            tma_load_3d(st + kWBoxBytes, &tmap_w, &w_full[ws], 64, (2 * kp + j) * kKStep, h);
-          }
+        for (int kb = 0; kb < kBoxesPerPart && ok; ++kb) {
           for (int p = 0; p < n && ok; ++p, ++q) {  // every part's [16 tokens][128 dims] box
             const uint32_t qs = q % kStages;
             if (!mbar_wait(&empty[qs], ((q / kStages) & 1) ^ 1, abort_s)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[qs], kBoxBytes);
-            tma_load_3d(smem + kMaRing + qs * kBoxBytes, &tmap_o, &full[qs], kp * kMaBoxDims, h,
+            tma_load_3d(smem + kMaRing + qs * kBoxBytes, &tmap_o, &full[qs], kb * kMaBoxDims, h,
                         (int32_t)((int64_t)p * a.T + t0));
           }
+        }
+      }
+    }
+  } else if (warp == kMaWProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer: w_vc K-steps
+    if (lane == 0) {
+      uint32_t wq = 0;  // w_vc K-steps issued so far
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        const int h = item / a.n_tiles;
+        for (int ks = 0; ks < kMaKSteps; ++ks, ++wq) {
+          const uint32_t ws = wq % kMaWStages;
+          if (!mbar_wait(&w_empty[ws], ((wq / kMaWStages) & 1) ^ 1, abort_s)) { ok = false; break; }
+          uint8_t* st = smem + kMaW + ws * kMaWStageBytes;
+          mbar_arrive_expect_tx(&w_full[ws], kMaWStageBytes);
+          tma_load_3d(st, &tmap_w, &w_full[ws], 0, ks * kKStep, h);
+          tma_load_3d(st + kWBoxBytes, &tmap_w, &w_full[ws], 64, ks * kKStep, h);
         }
       }
     }
@@ -521,49 +534,49 @@ __global__ void __launch_bounds__(kMaThreads, 1)
         break;
       }
       const float* w = wts + buf * kMaMaxParts * kMaTok;
-      for (int kp = 0; kp < kPairs && ok; ++kp) {
-        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+      for (int kb = 0; kb < kBoxesPerPart && ok; ++kb) {
+        float4 acc[kMaKPerBox];
+#pragma unroll
+        for (int j = 0; j < kMaKPerBox; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p = 0; p < n; ++p, ++q) {
           const uint32_t qs = q % kStages;
           if (!warp_wait_all(&full[qs], (q / kStages) & 1, abort_s)) { ok = false; break; }
           const float wp = w[p * kMaTok + r];
           const uint8_t* box = smem + kMaRing + qs * kBoxBytes;
-          float4 x0, x1;
-          if (kInBf16) {
-            const uint2 u0 = *reinterpret_cast<const uint2*>(box + r * kMaBoxDims * 2 + c4 * 8);
-            const uint2 u1 = *reinterpret_cast<const uint2*>(box + r * kMaBoxDims * 2 + 128 + c4 * 8);
-            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u0.x));
-            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u0.y));
-            const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u1.x));
-            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u1.y));
-            x0 = make_float4(a0.x, a0.y, b0.x, b0.y);
-            x1 = make_float4(a1.x, a1.y, b1.x, b1.y);
-          } else {
-            x0 = *reinterpret_cast<const float4*>(box + r * kMaBoxDims * 4 + c4 * 16);
-            x1 = *reinterpret_cast<const float4*>(box + r * kMaBoxDims * 4 + 256 + c4 * 16);
+          float4 x[kMaKPerBox];  // dims [64 j + 4 c4, +4) of K-step j of the box
+#pragma unroll
+          for (int j = 0; j < kMaKPerBox; ++j) {
+            if (kInBf16) {
+              const uint2 u = *reinterpret_cast<const uint2*>(box + r * kMaBoxDims * 2 + j * 128 + c4 * 8);
+              const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+              const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+              x[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+              x[j] = *reinterpret_cast<const float4*>(box + r * kMaBoxDims * 4 + j * 256 + c4 * 16);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[qs]);
-          acc0.x = fmaf(wp, x0.x, acc0.x); acc0.y = fmaf(wp, x0.y, acc0.y);
-          acc0.z = fmaf(wp, x0.z, acc0.z); acc0.w = fmaf(wp, x0.w, acc0.w);
-          acc1.x = fmaf(wp, x1.x, acc1.x); acc1.y = fmaf(wp, x1.y, acc1.y);
-          acc1.z = fmaf(wp, x1.z, acc1.z); acc1.w = fmaf(wp, x1.w, acc1.w);
+#pragma unroll
+          for (int j = 0; j < kMaKPerBox; ++j) {
+            acc[j].x = fmaf(wp, x[j].x, acc[j].x); acc[j].y = fmaf(wp, x[j].y, acc[j].y);
+            acc[j].z = fmaf(wp, x[j].z, acc[j].z); acc[j].w = fmaf(wp, x[j].w, acc[j].w);
+          }
         }
         if (!ok) break;
-        // K-steps 2 kp and 2 kp + 1 of the merged rows -> bf16, swizzled K-major:
+        // the box's K-steps of the merged rows -> bf16, swizzled K-major:
         // 16-byte chunk c16 of row r at r * 128 + ((c16 ^ (r % 8)) * 16)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float4 y = j ? acc1 : acc0;
-          const uint32_t off = kMaB + (buf * kMaKSteps + 2 * kp + j) * kMaBTileBytes + r * 128 +
+        for (int j = 0; j < kMaKPerBox; ++j) {
+          const uint32_t off = kMaB + (buf * kMaKSteps + kMaKPerBox * kb + j) * kMaBTileBytes + r * 128 +
                                ((((c4 >> 1) ^ (r & 7))) << 4) + (c4 & 1) * 8;
-          st_shared_v2(smem_u32(smem) + off, pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+          st_shared_v2(smem_u32(smem) + off, pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j].z, acc[j].w));
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&b_full[buf * kMaKSteps + 2 * kp]);
-          mbar_arrive(&b_full[buf * kMaKSteps + 2 * kp + 1]);
+#pragma unroll
+          for (int j = 0; j < kMaKPerBox; ++j) mbar_arrive(&b_full[buf * kMaKSteps + kMaKPerBox * kb + j]);
         }
       }
       if (!ok) break;
@@ -716,7 +729,11 @@ int32_t launch_merge_absorb(const CUtensorMap& to, const CUtensorMap& tw, const 
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess)
     return DCP_ERR_CUDA;
-  const int grid = a.n_items < sms ? a.n_items : sms;  // persistent: one CTA per SM
+  // persistent, at most one CTA per SM: the fewest CTAs that still give each the
+  // same largest share of items (384 items on 152 SMs: 128 CTAs of 3, not 152
+  // CTAs of 2 or 3), so that no SM's bandwidth goes to a short share
+  const int per_cta = (a.n_items + sms - 1) / sms;
+  const int grid = (a.n_items + per_cta - 1) / per_cta;
   merge_absorb_kernel<kInBf16, kBase2><<<grid, kMaThreads, kMaBytes, st>>>(to, tw, a);
   return launch_status();
 }
