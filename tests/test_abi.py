@@ -218,6 +218,52 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert absorb_o(o=None) == -1
     assert absorb_o(v=P(1032)) == -1
     assert absorb_o(H=0) == -1
+    # the merge and the output product in one call
+
+    def merge_absorb(n=8, T=4, H=8, o=P(256), od=0, lp=P(256), base=1, w=P(512), v=P(1024), vd=1):
+        return lib.dcp_lse_merge_absorb_o(n, T, H, o, od, lp, base, w, v, vd, None, None, None)
+    assert merge_absorb(T=0) == 0                   # no-op, nothing launched
+    assert merge_absorb(n=0) == -1
+    assert merge_absorb(n=65) == -1                 # more parts than the kernel's weight buffers hold
+    assert merge_absorb(T=-1) == -1
+    assert merge_absorb(H=0) == -1
+    assert merge_absorb(H=65536) == -1
+    assert merge_absorb(od=2) == -1
+    assert merge_absorb(vd=7) == -1
+    assert merge_absorb(base=2) == -1
+    assert merge_absorb(lp=None) == -1
+    assert merge_absorb(w=P(520)) == -1             # not 16-byte aligned
+    # the exchange of the partials over W ranks
+    assert lib.dcp_a2a_chunk_bytes(1, 64, 96, 8, 1) > 0
+    assert lib.dcp_a2a_chunk_bytes(1, 64, 96, 7, 1) == 0    # heads do not split evenly
+    assert lib.dcp_a2a_chunk_bytes(0, 64, 96, 8, 1) == 0
+    assert lib.dcp_a2a_chunk_bytes(1, 64, 96, 8, 5) == 0
+
+    def pack(nh=1, T=4, H=8, W=2, o=P(256), od=0, lp=P(256), send=P(1024), wd=1):
+        return lib.dcp_pack_partials(nh, T, H, W, o, od, lp, send, wd, None)
+    assert pack(T=0) == 0
+    assert pack(W=3) == -1
+    assert pack(od=4) == -1
+    assert pack(send=None) == -1
+    assert pack(o=P(264)) == -1
+
+    def merge_packed(W=2, nh=1, rows=16, recv=P(1024), wd=1, base=0, o=P(256), od=1):
+        return lib.dcp_lse_merge_packed(W, nh, rows, recv, wd, base, o, od, None, None)
+    assert merge_packed(rows=0) == 0
+    assert merge_packed(W=0) == -1
+    assert merge_packed(nh=0) == -1
+    assert merge_packed(base=3) == -1
+    assert merge_packed(recv=None) == -1
+    assert merge_packed(o=P(260)) == -1
+
+    def rescale(N=8, sb=0, nh=4, T=4, H=8, W=2, la=P(256), o=P(512), od=0, base=0, os=P(1024)):
+        return lib.dcp_lse_rescale(N, sb, nh, T, H, W, la, o, od, base, os, None, None)
+    assert rescale(T=0) == 0
+    assert rescale(sb=6) == -1                      # shards [6, 10) past the 8 shards
+    assert rescale(W=3) == -1
+    assert rescale(base=5) == -1
+    assert rescale(la=None) == -1
+    assert rescale(os=P(1028)) == -1
 
 
 def test_package_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -6,7 +6,7 @@ core multiplies bf16 by bf16), so v is compared with the oracle on the exact
 merged o within the rounding bound of that operand, 2^-8 sum_k |o_k w_kn|, plus
 the bf16 output rounding when v is bf16; lse within 1e-5 of the oracle's merge.
 Cases: the K3 shapes (8 parts, 64 tokens, 96 heads, base 2), 16 parts, one
-part, token tails (1, 33, 300 tokens: partial, one and ten 32-token tiles),
+part, 64 parts (the most the call takes), token tails (1, 33, 300 tokens: partial, one and ten 32-token tiles),
 bf16 partials, empty parts (lse = -inf) and a row whose parts are all empty,
 and the absorbed decode layer end to end.
 """
@@ -75,7 +75,7 @@ def test_merge_absorb_k3_shapes(part_dtype, v_dtype, base):
     check(v, lse_out, o, lse, w_vc, base, f"k3 {part_dtype}->{v_dtype} base {base}")
 
 
-@pytest.mark.parametrize("n,T,H", [(16, 33, 5), (1, 300, 2), (8, 1, 3), (3, 64, 1)])
+@pytest.mark.parametrize("n,T,H", [(16, 33, 5), (1, 300, 2), (8, 1, 3), (3, 64, 1), (64, 20, 2)])
 def test_merge_absorb_token_tails_and_part_counts(n, T, H):
     g = torch.Generator().manual_seed(n * 1000 + T)
     w_vc = (torch.randn(H, 512, 128, generator=g) / 512 ** 0.5).to(torch.bfloat16)
