@@ -6,8 +6,8 @@ core multiplies bf16 by bf16), so v is compared with the oracle on the exact
 merged o within the rounding bound of that operand, 2^-8 sum_k |o_k w_kn|, plus
 the bf16 output rounding when v is bf16; lse within 1e-5 of the oracle's merge.
 Cases: the K3 shapes (8 parts, 64 tokens, 96 heads, base 2), 16 parts, one
-part, 64 parts (the most the call takes), token tails (1, 33, 300 tokens: partial, one and ten 32-token tiles),
-bf16 partials, empty parts (lse = -inf) and a row whose parts are all empty,
+part, 64 parts (the most the call takes), token tails of 1, 20, 33 and 300
+tokens (the kernel's items are 16 tokens of one head), bf16 partials, empty parts (lse = -inf) and a row whose parts are all empty,
 and the absorbed decode layer end to end.
 """
 
