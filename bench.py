@@ -257,12 +257,18 @@ def run_ours(args, cfg, rank, world, dist, device):
                for _ in range(args.steps)]
     ev_part = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+    ev_app = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
 
     local = dec.local if group else dec
 
     def step(i=None):
         if st["kv_new"] is not None:
+            if i is not None:
+                ev_app[i][0].record(stream)
             dec.append(st["kv_new"], st["pos"], st["req"], st["bt"])
+            if i is not None:
+                ev_app[i][1].record(stream)
         if i is not None:
             ev_part[i][0].record(stream)
         local.partial(st["q"], st["bt"], st["seq_lens"])
@@ -303,6 +309,17 @@ def run_ours(args, cfg, rank, world, dist, device):
         raise RuntimeError(f"device status {dec.status_bits()} after the timed steps")
     ms_per_step = max_over_ranks(dist, total_ms / args.steps)
     part_ms_avg = max_over_ranks(dist, sum(part_ms) / len(part_ms))
+    append = None
+    if st["kv_new"] is not None:
+        # the owner-filtered append of the step's new rows, on its own: each row is
+        # read once (1152 B + its position and request) and written once by its owner
+        app_ms = max_over_ranks(dist, statistics.mean(a.elapsed_time(b) for a, b in ev_app))
+        rows = st["kv_new"].shape[0]
+        append = {"rows": rows, "us": round(app_ms * 1e3, 2),
+                  "note": "dcp_kv_append alone (CUDA events around it inside the timed steps)"}
+        if not group:
+            app_bytes = rows * (2 * KV_ROW_BYTES + 12)
+            append.update({"bytes": app_bytes, "GB/s": round(app_bytes / (app_ms * 1e-3) / 1e9, 1)})
 
     # end-to-end through the public API with host buffers (H2D inputs, D2H result each step)
     e2e = None
@@ -349,6 +366,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         "config": config_dict(cfg, st["S"], world, args.exchange if group else None),
         "roofline": roof,
         "partial_ms": round(part_ms_avg, 5),
+        "append": append,
         "step_ms_median": round(statistics.median(step_ms), 5),
         "gpu_launches": launches,
         "e2e": e2e,
