@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 // shared memory as a bf16 operand and multiplied by w_vc[h] on the tensor core;
 // only v (and the merged lse) is written.  The merged o never reaches global
 // memory.
-// Persistent: one CTA per SM walks the work items, its warps in six roles:
+// Persistent: at most one CTA per SM walks the work items (the grid is the
+// fewest CTAs that still give each the largest share), its warps in six roles:
 //   producers (warps 12 and 15, one thread each)  stream, two K-steps at a
 //        time, each part's [16 tokens][128 dims] box of o_part by TMA into a
 //        ring of shared-memory stages (144 KB in flight), and, on their own,
