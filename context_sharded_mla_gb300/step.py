@@ -5,6 +5,12 @@ this GPU (the pools of shards [shard_begin, shard_end), the partial outputs,
 the merged output and the library workspace), all allocated once through
 PyTorch.  Each method is a fixed sequence of C-ABI calls; no arithmetic of the
 method happens here.
+
+The library's host work per call depends only on shapes, pointers and the
+device (every length is read on the device), and nothing here synchronises or
+allocates per call, so a whole ``step`` can be captured once in a CUDA graph
+(``torch.cuda.graph``) and replayed with new lengths, queries and rows written
+in place into the captured tensors.
 """
 
 from __future__ import annotations
