@@ -330,25 +330,26 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
   }
 }
 
-// v[idx] for idx in 0..3, without indexing registers at run time
-__device__ __forceinline__ uint32_t sel4(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, int idx) {
-  const uint32_t lo = (idx & 1) ? v1 : v0, hi = (idx & 1) ? v3 : v2;
-  return (idx & 2) ? hi : lo;
-}
-
 // The same O rows times `inv` -> the output rows (bf16 or fp32) or the fp32
 // piece rows; thread t holds dims [d0, d0 + 128) of row r0 + t % 16.  Rows
 // [0, rows_here) of the group are written.  Kept out of line: it runs once per
 // segment and inlining it cost the tile loop.
 //
-// fp32 rows: per 32 dims, the four lanes of each lane group (4 rows) trade
-// 32-byte blocks by shuffles (each lane offers a rotated block, then picks)
-// so that the group writes 128 contiguous bytes of one row per pair of stores.
-// bf16 rows: one row per lane.  All stores are 16 bytes wide: a 32-byte
+// fp32 rows go through `stage`, this warp's 16 rows of the score-exchange
+// buffer it read the peer's last tile from (4 KB: 64 floats per row, 16-byte
+// chunk c of row r at chunk slot c ^ (r % 16), as the exchange lays them out);
+// nothing writes those rows again before this warp ships its next tile.  Per 32
+// dims, each thread writes its row segment (128 bytes) there, and the warp reads
+// them back so that 8 lanes hold one segment: each store instruction writes 4
+// whole 128-byte lines.  (Each lane storing its own row touches 32 lines per
+// instruction and took about twice as long; a shuffle transpose among lane
+// groups of 4 touches 8 and spends more in shuffles than the staging costs.)
+// bf16 rows: one row per lane.  All global stores are 16 bytes wide: a 32-byte
 // st.global.v8 in this routine was found to land only its first word in one
 // build of the kernel.
 __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int rows_here, bool whole,
-                                          int64_t out_base, int64_t piece_base, int r0, int d0, float inv) {
+                                          int64_t out_base, int64_t piece_base, int r0, int d0, float inv,
+                                          uint32_t stage) {
   const int lane = threadIdx.x & 31;
   const int row = r0 + (lane & 15);
   if (whole && a.o_bf16) {
@@ -370,35 +371,28 @@ __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int 
     return;
   }
   float* const out0 = whole ? static_cast<float*>(a.o_part) + out_base * kDv : a.piece_o + piece_base * kDv;
-  const int p = lane & 3, gl = lane & ~3;
+  const int h = lane >> 4, lr = lane & 15;          // this thread's half-row and row within the warp
+  const int dbase = d0 - 128 * h;                   // this CTA's first dim
+  const int c = lane & 7;                           // read-back: chunk c of segment 4 i + lane / 8
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
     uint32_t rr[32];
     tmem_ld16x2_sync<128>(o_addr + 32 * k, rr);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * inv);
-    // step s: lane p offers its block (p + s) & 3 and takes block p of lane (p - s) & 3
-    uint32_t got[4][8];
+    for (int i = 0; i < 8; ++i)
+      st_shared_v4(stage + (uint32_t)lr * kXRowBytes + ((uint32_t)((8 * h + i) ^ lr) << 4),
+                   __float_as_uint(__uint_as_float(rr[4 * i]) * inv), __float_as_uint(__uint_as_float(rr[4 * i + 1]) * inv),
+                   __float_as_uint(__uint_as_float(rr[4 * i + 2]) * inv), __float_as_uint(__uint_as_float(rr[4 * i + 3]) * inv));
+    __syncwarp();
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int ob = (p + s) & 3, src = gl | ((p - s) & 3);
-#pragma unroll
-      for (int w = 0; w < 8; ++w)
-        got[s][w] = __shfl_sync(0xffffffffu, sel4(rr[w], rr[8 + w], rr[16 + w], rr[24 + w], ob), src);
+    for (int i = 0; i < 8; ++i) {
+      const int sg = 4 * i + (lane >> 3);           // segment: row sg / 2, half sg % 2
+      const int sr = sg >> 1, sh = sg & 1;
+      const uint4 v = ld_shared_v4(stage + (uint32_t)sr * kXRowBytes + ((uint32_t)((8 * sh + c) ^ sr) << 4));
+      if (r0 + sr < rows_here)
+        *reinterpret_cast<uint4*>(out0 + (int64_t)(r0 + sr) * kDv + dbase + 128 * sh + 32 * k + 4 * c) = v;
     }
-    // row of lane gl + q: its block p came at step (p - q) & 3
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int rq = r0 + ((gl | q) & 15), s = (p - q) & 3;
-      uint32_t v8[8];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v8[w] = sel4(got[0][w], got[1][w], got[2][w], got[3][w], s);
-      if (rq < rows_here) {
-        float4* d4 = reinterpret_cast<float4*>(out0 + (int64_t)rq * kDv + d0 + 32 * k + 8 * p);
-        d4[0] = make_float4(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]), __uint_as_float(v8[3]));
-        d4[1] = make_float4(__uint_as_float(v8[4]), __uint_as_float(v8[5]), __uint_as_float(v8[6]), __uint_as_float(v8[7]));
-      }
-    }
+    __syncwarp();                                   // the reads are done before the next k's writes
   }
 }
 
@@ -984,8 +978,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int64_t piece_base = (int64_t)(2 * v + kslot) * a.R_total + g * Rg;
         const int64_t out_row = out_base + row, piece_row = piece_base + row;
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        // staging for the fp32 rows: this warp's rows of the buffer the last tile's
+        // peer scores were read from
         store_o_rows(a, tmem + lane_addr + kOCol, rows_here, whole, out_base, piece_base, r0, 256 * (int)rank + 128 * h,
-                     inv);
+                     inv, smem_u32(x_s) + ((jl & 1) ^ 1) * sl.xbuf + (uint32_t)r0 * kXRowBytes);
         if (writes && h == 0 && rank == 0) {
           const float lse2 = l_row > 0.f ? m_ref + log2f(l_row) : -INFINITY;
           if (whole)
