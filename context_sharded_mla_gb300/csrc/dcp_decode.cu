@@ -615,17 +615,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+      // A segment's length and the page ids of its first 32 tiles are loaded
+      // during the segment before it, so that a segment start waits on no
+      // global load.  The early page ids are read without the length (up to
+      // max_pages entries of the row); to_rows applies the length when they are
+      // used.
+      bool have = it.next(&u, &t0, &nt, &whole, &kslot);
+      int32_t pgf[8];       // page ids of the boxes of the segment's first 32 tiles
+      int64_t nvis_f = 0;   // and its visible rows
+      if (have) {
+        bool bad0 = false;
+        nvis_f = unit_nvis_max(a, u / a.n_held, u % a.n_held, &bad0);
+        fetch_batch(u / a.n_held, INT64_MAX, t0, t0 + nt, pgf);
+      }
+      while (ok && have) {
         const int b = u / a.n_held, rs = u % a.n_held;
-        bool bad = false;
-        const int64_t nvis = unit_nvis_max(a, b, rs, &bad);
+        const int64_t nvis = nvis_f;
         const int32_t t_end = t0 + nt;
         // block-table entries of the next 32 tiles are in flight while the
         // current 32 are issued; each lane turns its tile's entries into TMA rows
         int32_t pgn[8], yc[8], yn = -1;  // yn: next batch's first-box rows (L2 prefetch)
-        fetch_batch(b, nvis, t0, t_end, pgn);
-        to_rows(rs, t0, t_end, nvis, pgn, yc);
+        to_rows(rs, t0, t_end, nvis, pgf, yc);
         fetch_batch(b, nvis, t0 + 32, t_end, pgn);
+        // the next segment, peeked once this segment's first tile is issued (the
+        // peek waits on the unit table): its length and first page ids are then
+        // in flight during this segment
+        SegIter nx = it;
+        int32_t u2 = 0, t02 = 0, nt2 = 0, ks2 = 0;
+        bool wh2 = false, has_next = false;
+        int32_t y_next = -1;    // first-box row of the next segment's tile `lane` (L2 prefetch)
+        bool next_rows = false;
         // the query's chunk 4r + 3 and its rope dims [32r, 32r + 32) for the SS part of QK
         if (!warp_wait(&bars[kQEmpty], (seg & 1) ^ 1, abort_s, lane)) { ok = false; break; }
         if (lane == 0) {
@@ -659,6 +678,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_prefetch_3d(&tmap_kv4, 0, ya, kOwnChunks * (int)rank);
               tma_prefetch_2d(&tmap_kv64, 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, ya);
             }
+            // past this segment's end: the next segment's first tiles
+            if (ja >= nt && has_next && ja - nt < nt2 && ja - nt < 32) {
+              if (!next_rows) {
+                int32_t yt[8];
+                to_rows_quiet(u2 % a.n_held, t02, pgf, yt);
+                y_next = yt[0];
+                next_rows = true;
+              }
+              const int32_t yb = __shfl_sync(0xffffffffu, y_next, ja - nt);
+              if (lane == 0 && yb >= 0) {
+                tma_prefetch_3d(&tmap_kv4, 0, yb, kOwnChunks * (int)rank);
+                tma_prefetch_2d(&tmap_kv64, 2 * kOwnChunks * kChunkDims + kRopeHalf * (int)rank, yb);
+              }
+            }
           }
           Boxes cur;
           if (nbox == 1) {
@@ -671,7 +704,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             make_boxes(y, cur);
           }
           ok = load_tile(cur);
+          if (jj == 0) {
+            has_next = nx.next(&u2, &t02, &nt2, &wh2, &ks2);
+            if (has_next) {
+              bool bad2 = false;
+              nvis_f = unit_nvis_max(a, u2 / a.n_held, u2 % a.n_held, &bad2);
+              fetch_batch(u2 / a.n_held, INT64_MAX, t02, t02 + nt2, pgf);
+            }
+          }
         }
+        it = nx;  // the segment just peeked (its fields below)
+        have = has_next;
+        u = u2, t0 = t02, nt = nt2, whole = wh2, kslot = ks2;
       }
       // Drain: every slot's last release (a tensor-core commit) lands before the
       // CTA may retire.  Bounded; skipped after an abort.
@@ -855,19 +899,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       bool q_next = false;  // the next segment's query is already in TMEM
-      while (ok && it.next(&u, &t0, &nt, &whole, &kslot)) {
+      // Each segment's description and length come from the segment before it
+      // (peeked and loaded there), so a segment start waits on no global load.
+      bool have = it.next(&u, &t0, &nt, &whole, &kslot);
+      int64_t S_cur = have ? a.seq_lens[u / a.n_held] : 0;
+      while (ok && have) {
         const int b = u / a.n_held, rs = u % a.n_held;
         if (!q_next && !load_q(b, seg)) { ok = false; break; }
         q_next = false;
         ++seg;
-        // The next segment: its query rows into L2 now, into TMEM before this
-        // segment's epilogue, so that its first QK product overlaps the epilogue.
+        // The next segment, peeked once this segment's first tile is done (the
+        // peek waits on the unit table): its length is loaded then, its query
+        // rows go into L2 then and into TMEM before this segment's epilogue, so
+        // that its first QK product overlaps the epilogue.
         SegIter nx = it;
-        int32_t u2, t02, nt2, ks2;
-        bool wh2;
-        const bool has_next = nx.next(&u2, &t02, &nt2, &wh2, &ks2);
-        if (has_next && has_row) asm volatile("prefetch.global.L2 [%0];" ::"l"(q_src(u2 / a.n_held)));
-        const int64_t S = a.seq_lens[b];
+        int32_t u2 = 0, t02 = 0, nt2 = 0, ks2 = 0;
+        bool wh2 = false, has_next = false;
+        int64_t S_next = 0;
+        const int64_t S = S_cur;
         int64_t nvis = 0;  // keys of this shard visible to the row
         if (has_row && S >= a.q_len) nvis = count_of(a.shard_begin + rs, S - a.q_len + grow / a.H + 1, a.L);
         float m_ref = -INFINITY;  // running maximum of the row (log2 units)
@@ -961,6 +1010,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kPFull0 + bsel]);
+          if (jj == 0) {
+            has_next = nx.next(&u2, &t02, &nt2, &wh2, &ks2);
+            if (has_next) {
+              S_next = a.seq_lens[u2 / a.n_held];
+              if (has_row) asm volatile("prefetch.global.L2 [%0];" ::"l"(q_src(u2 / a.n_held)));
+            }
+          }
         }
         if (!ok) break;
         if (has_next) {
@@ -992,6 +1048,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kOFree]);
+        it = nx;  // the segment just peeked (its fields below)
+        have = has_next;
+        u = u2, t0 = t02, nt = nt2, whole = wh2, kslot = ks2;
+        S_cur = S_next;
       }
     }
   }
