@@ -181,7 +181,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_state(cfg, device, rank=0, world=1, strategy=None):
+def build_state(cfg, device, rank=0, world=1, strategy=None, part_dtype=torch.float32):
     """The workload's cache appended into this rank's decoder: all N shards on one
     GPU (world == 1), or, with a DCP group, this rank's N / world shards."""
     import context_sharded_mla_gb300 as dcp
@@ -195,11 +195,11 @@ def build_state(cfg, device, rank=0, world=1, strategy=None):
     base = dcp.DCP_LSE_BASE_2 if cfg.base == 2 else dcp.DCP_LSE_BASE_E
     if strategy is None:
         dec = ShardedMlaDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, base,
-                                out_dtype, torch.float32, device=device)
+                                out_dtype, part_dtype, device=device)
     else:
         from context_sharded_mla_gb300.group import DcpGroupDecoder
         dec = DcpGroupDecoder(lay, cfg.B, cfg.q_len, cfg.H, pool_pages, bt.shape[1], workloads.SCALE, rank, world,
-                              base, strategy, torch.bfloat16, out_dtype, torch.float32, device=device)
+                              base, strategy, torch.bfloat16, out_dtype, part_dtype, device=device)
     btd = bt.to(device)
     # cache: every request holds S_b - new tokens before the step; the step appends the rest
     new_rows, new_pos, new_req = [], [], []
@@ -241,7 +241,8 @@ def run_ours(args, cfg, rank, world, dist, device):
         # split H / world per GPU after the exchange; total work fixed (strong scaling)
         if cfg.N % world or cfg.H % world:
             raise SystemExit(f"{cfg.name}: {cfg.N} shards and {cfg.H} heads must split evenly over {world} GPUs")
-    st = build_state(cfg, device, rank, world, args.exchange if group else None)
+    part_dtype = torch.bfloat16 if args.partials == "bf16" else torch.float32
+    st = build_state(cfg, device, rank, world, args.exchange if group else None, part_dtype)
     dec = st["dec"]
     acct = workload_accounting(cfg, st["S"])
     if group:
@@ -340,7 +341,8 @@ def run_ours(args, cfg, rank, world, dist, device):
     else:
         roof = {"bound": "tensor", "achieved": round(part_flops, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(part_flops / peaks["bf16_tflops"], 4)}
-    roof["traffic"] = recorded_traffic(cfg.name) if args.batch is None else None
+    # the committed captures are of the default launch (full batch, fp32 partials)
+    roof["traffic"] = recorded_traffic(cfg.name) if args.batch is None and args.partials == "fp32" else None
     roof["kernel"] = "dcp_mla_decode_partial (all its launches, CUDA events on the launching stream)"
     roof["peak_source"] = f"{peaks['source']} MEASURED_PEAKS.json" if peaks["source"] == "measured" else "fallback"
     if group:
@@ -363,7 +365,7 @@ def run_ours(args, cfg, rank, world, dist, device):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 latent rows and queries, shuffled block table)",
-        "config": config_dict(cfg, st["S"], world, args.exchange if group else None),
+        "config": config_dict(cfg, st["S"], world, args.exchange if group else None, args.partials),
         "roofline": roof,
         "partial_ms": round(part_ms_avg, 5),
         "append": append,
@@ -801,13 +803,13 @@ def recorded_traffic(key):
         return None
 
 
-def config_dict(cfg, S, world, strategy=None):
+def config_dict(cfg, S, world, strategy=None, partials="fp32"):
     """The decode step's `config`, from the workload alone (both arms print the same one)."""
     d = {"workload": workloads.DESCRIPTIONS[cfg.name] if cfg.name in workloads.DESCRIPTIONS else cfg.name,
          "B": cfg.B, "H": cfg.H, "q_len": cfg.q_len, "S_total": int(S.sum()), "S_max": int(S.max()),
          "n_shards": cfg.N, "interleave": cfg.I, "page_size": cfg.P, "lse_base": "2" if cfg.base == 2 else "e",
          "new_tokens_per_request": max(cfg.append, cfg.chunk), "out_dtype": cfg.out_dtype,
-         "partials": "fp32", "global_batch": cfg.B, "seq_len": int(S.max()),
+         "partials": partials, "global_batch": cfg.B, "seq_len": int(S.max()),
          "parallelism": ("1 GPU holds all N shards" if strategy is None else
                          f"DCP over {world} GPUs: {cfg.N // world} shards and {cfg.H // world} output heads per GPU, "
                          f"query replicated, {strategy} exchange of the partials"),
@@ -919,7 +921,8 @@ def run_reference(args, cfg, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "strong" if world > 1 or args.group else "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": config_dict(cfg, workloads.lengths(cfg), world, args.exchange if world > 1 or args.group else None),
+        "config": config_dict(cfg, workloads.lengths(cfg), world, args.exchange if world > 1 or args.group else None,
+                              args.partials),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -962,6 +965,9 @@ def parse(argv=None):
     ap.add_argument("--workload", default="k3", choices=sorted(workloads.DESCRIPTIONS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller case for profiling)")
+    ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype of the per-shard partial outputs o_r (fp32 by default; bf16 is the all-to-all "
+                         "wire format of the pages)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
