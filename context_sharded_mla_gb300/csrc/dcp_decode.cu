@@ -344,36 +344,53 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f) {
 // whole 128-byte lines.  (Each lane storing its own row touches 32 lines per
 // instruction and took about twice as long; a shuffle transpose among lane
 // groups of 4 touches 8 and spends more in shuffles than the staging costs.)
-// bf16 rows: one row per lane.  All global stores are 16 bytes wide: a 32-byte
+// bf16 rows go the same way, two 32-dim blocks (128 bytes) per thread at a
+// time.  All global stores are 16 bytes wide: a 32-byte
 // st.global.v8 in this routine was found to land only its first word in one
 // build of the kernel.
 __device__ __noinline__ void store_o_rows(const TcArgs& a, uint32_t o_addr, int rows_here, bool whole,
                                           int64_t out_base, int64_t piece_base, int r0, int d0, float inv,
                                           uint32_t stage) {
   const int lane = threadIdx.x & 31;
-  const int row = r0 + (lane & 15);
+  const int h = lane >> 4, lr = lane & 15;          // this thread's half-row and row within the warp
+  const int dbase = d0 - 128 * h;                   // this CTA's first dim
+  const int c = lane & 7;                           // read-back: chunk c of segment 4 i + lane / 8
   if (whole && a.o_bf16) {
+    // bf16 rows, staged like the fp32 ones: two 32-dim blocks (128 bytes) per
+    // thread at a time
+    __nv_bfloat16* const outb = static_cast<__nv_bfloat16*>(a.o_part) + out_base * kDv;
 #pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-      uint32_t rr[32];
-      tmem_ld16x2_sync<128>(o_addr + 32 * k, rr);
-      if (row >= rows_here) continue;
-      uint32_t w[16];
+    for (int kp = 0; kp < 2; ++kp) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {        // each 32-dim block: 4 of the row segment's 8 chunks
+        uint32_t rr[32];
+        tmem_ld16x2_sync<128>(o_addr + 32 * (2 * kp + half), rr);
+        uint32_t w[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
-        w[e] = *reinterpret_cast<uint32_t*>(&hh);
+        for (int e = 0; e < 16; ++e) {
+          __nv_bfloat162 hh =
+              __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
+          w[e] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_shared_v4(stage + (uint32_t)lr * kXRowBytes + ((uint32_t)((8 * h + 4 * half + i) ^ lr) << 4), w[4 * i],
+                       w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
-      uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_part) + (out_base + row) * kDv + d0 + 32 * k);
+      __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < 8; ++i) {
+        const int sg = 4 * i + (lane >> 3);         // segment: row sg / 2, half sg % 2
+        const int sr = sg >> 1, sh = sg & 1;
+        const uint4 v = ld_shared_v4(stage + (uint32_t)sr * kXRowBytes + ((uint32_t)((8 * sh + c) ^ sr) << 4));
+        if (r0 + sr < rows_here)
+          *reinterpret_cast<uint4*>(outb + (int64_t)(r0 + sr) * kDv + dbase + 128 * sh + 64 * kp + 8 * c) = v;
+      }
+      __syncwarp();
     }
     return;
   }
   float* const out0 = whole ? static_cast<float*>(a.o_part) + out_base * kDv : a.piece_o + piece_base * kDv;
-  const int h = lane >> 4, lr = lane & 15;          // this thread's half-row and row within the warp
-  const int dbase = d0 - 128 * h;                   // this CTA's first dim
-  const int c = lane & 7;                           // read-back: chunk c of segment 4 i + lane / 8
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
     uint32_t rr[32];
