@@ -124,10 +124,18 @@ def test_running_max_jumps(H, N):
             assert_close_lse(to_f64(dec.lse_part[r, b]), rlp[r], f"jump lse_part r={r}")
 
 
-def test_bf16_partials():
-    cfg = workloads.config("k3", **SMALL["k3"])
-    st = GpuState(cfg, part_dtype=torch.bfloat16)
-    _check_state(st, rel_bound=2e-2)
+@pytest.mark.parametrize("name,over", [
+    ("k3", SMALL["k3"]),                                    # 96 rows: every softmax warp full
+    ("k3", dict(B=3, S=3000 + 9, H=40)),                    # 40 rows in a 48-row group: a warp with 8 rows
+    ("ragged", dict(B=4, S=2500, S_min=40, H=5)),           # 20 rows (q_len 4 x 5 heads): a warp with 4 rows
+])
+@pytest.mark.parametrize("part_dtype", [torch.bfloat16, torch.float32])
+def test_partial_rows_of_both_dtypes(name, over, part_dtype):
+    """The epilogue writes each warp's rows through shared memory; groups whose
+    last warp has fewer than 16 rows must write only those rows."""
+    cfg = workloads.config(name, **over)
+    st = GpuState(cfg, part_dtype=part_dtype)
+    _check_state(st, rel_bound=2e-2 if part_dtype == torch.bfloat16 else None)
 
 
 @pytest.mark.parametrize("N,I,P,q_len", [(16, 16, 64, 4), (8, 1, 64, 1), (4, 2, 16, 4)])
