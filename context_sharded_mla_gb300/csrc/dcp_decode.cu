@@ -433,6 +433,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) flag(a.status, DCP_STATUS_INTERNAL);
     return;
   }
+  // launched as a programmatic dependent of the plan kernel: nothing it wrote
+  // (the tile prefix sums, the empty units' rows) is read before this
+  griddep_wait();
   unsigned char* smem = smem_raw;
   const SmemLayout sl = smem_layout(a.Rg, a.nts);
   unsigned char* qc_s = smem + sl.qc;
@@ -1114,6 +1117,7 @@ constexpr int kFixupRows = kFixupThreads / 32;  // query rows per block: one per
 __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(TcArgs a) {
   __shared__ int32_t piece_s[kMaxPieces];
   __shared__ int32_t npiece_s, unit_s;
+  griddep_wait();  // a programmatic dependent of the partial kernel: its pieces are complete after this
   const int32_t U = a.B * a.n_held;
   const int V = a.V;
   const int64_t T = a.tile_start[U];
@@ -1438,13 +1442,32 @@ int32_t launch_decode(const Plan& p, const dcp_layout_t* layout, int32_t shard_b
   cudaStream_t st = as_stream(stream);
   const int32_t U = B * n_held;
   plan_kernel<<<1, 1024, 0, st>>>(a, reinterpret_cast<int32_t*>(ws), U);
-  partial_tc_kernel<<<2 * p.V * p.ngroups, kThreads, p.smem, st>>>(tq, tkv, tq64, tkv64, tkv4, a);
+  // The partial kernel and the fixup are programmatic dependent launches: each
+  // grid may be scheduled while the one before it finishes, and waits
+  // (griddepcontrol.wait) before it reads anything that one wrote.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)(2 * p.V * p.ngroups));
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = p.smem;
+  lc.stream = st;
+  lc.attrs = pdl;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, partial_tc_kernel, tq, tkv, tq64, tkv64, tkv4, a) != cudaSuccess) return DCP_ERR_CUDA;
   // Cut units need their pieces merged: one block column per range boundary,
   // one warp per row up to 96 rows, blocks looping over further row chunks.
   // With one range per row group nothing is cut and no fixup runs.
   if (p.V > 1) {
     const unsigned fix_y = (unsigned)std::min((a.R_total + kFixupRows - 1) / kFixupRows, 12);
-    fixup_kernel<<<dim3((unsigned)(p.V - 1), fix_y), kFixupThreads, 0, st>>>(a);
+    cudaLaunchConfig_t lf = {};
+    lf.gridDim = dim3((unsigned)(p.V - 1), fix_y);
+    lf.blockDim = dim3(kFixupThreads);
+    lf.stream = st;
+    lf.attrs = pdl;
+    lf.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lf, fixup_kernel, a) != cudaSuccess) return DCP_ERR_CUDA;
     return launch_status(3);
   }
   return launch_status(2);

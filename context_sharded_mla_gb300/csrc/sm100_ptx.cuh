@@ -264,6 +264,12 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&r)[
       : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Wait until the grids this one depends on in the stream have completed and
+// their writes are visible.  With a programmatic dependent launch the grid may
+// start while the one before it finishes; without one this returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
