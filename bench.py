@@ -1002,11 +1002,6 @@ def main(argv=None):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     os.environ.setdefault("NCCL_NVLS_ENABLE", "0")   # plain NVLink transfers, no multicast objects
-    if world > 1:
-        # NCCL's communicator set-up lines on stderr: the record shows which
-        # transport each rank pair used (stdout keeps the one JSON line)
-        os.environ.setdefault("NCCL_DEBUG", "INFO")
-        os.environ.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
     dist = init_dist(world, "nccl")
     if args.op in ("relayout", "absorb"):
         run_op, time_op = ((run_relayout_op, time_oracle_relayout) if args.op == "relayout"
