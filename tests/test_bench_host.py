@@ -1,4 +1,4 @@
-"""Host logic of bench.py (no GPU): clock-sample windowing and the recorded-traffic lookup."""
+"""Host logic of bench.py (no GPU): clock-sample windowing, the recorded-traffic lookup and the reference arm's config."""
 
 import datetime
 import hashlib
@@ -48,3 +48,25 @@ def test_recorded_traffic_needs_the_captured_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("other") is None
     src.write_text("// kernel source, changed\n")          # the counters no longer describe this kernel
     assert bench.recorded_traffic("w") is None
+
+
+def test_reference_arm_prints_our_config(monkeypatch):
+    """The reference arm reports the same config as ours (the driver compares them),
+    for the default step and with the bf16-partials option.  The oracle's sample is
+    cut to a few rows so the test stays fast; its config does not depend on it."""
+    import numpy as np
+    import bench
+    import workloads
+    rng = np.random.default_rng(0)
+    monkeypatch.setattr(bench, "time_oracle_fraction",
+                        lambda cfg, s, device=None: (0, rng.standard_normal((1, 2, 576)),
+                                                     rng.standard_normal((40, 576)), 1, 40))
+    for argv in (["--impl", "reference", "--steps", "1", "--warmup", "1"],
+                 ["--impl", "reference", "--steps", "1", "--warmup", "1", "--partials", "bf16"],
+                 ["--impl", "reference", "--steps", "1", "--warmup", "1", "--workload", "dsv3"]):
+        args = bench.parse(argv)
+        cfg = workloads.config(args.workload)
+        out = bench.run_reference(args, cfg, 0, 1)
+        assert out["impl"] == "reference"
+        assert out["config"] == bench.config_dict(cfg, workloads.lengths(cfg), 1, None, args.partials)
+        assert out["metric"] == bench.METRIC and out["higher_is_better"] is True
