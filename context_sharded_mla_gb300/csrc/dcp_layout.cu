@@ -108,6 +108,11 @@ __global__ void kv_append_kernel(Layout L, int32_t shard_begin, int32_t shard_en
     row = local_row_of(p, L);
   }
   if (own < shard_begin || own >= shard_end) return;  // another device's shard
+  // the row's loads go out before the block-table lookup, so the two latencies
+  // overlap (the row is read whether or not its page turns out valid)
+  const uint4* src = kv_new + t * kVec;
+  uint4 v0 = __ldg(src + lane), v1 = __ldg(src + 32 + lane), v2 = make_uint4(0, 0, 0, 0);
+  if (lane < kVec - 64) v2 = __ldg(src + 64 + lane);
   const int64_t pidx = row / L.P;
   if (pidx >= max_pages) {
     if (lane == 0) flag(status, DCP_STATUS_BAD_PAGE_INDEX);
@@ -119,10 +124,7 @@ __global__ void kv_append_kernel(Layout L, int32_t shard_begin, int32_t shard_en
     return;
   }
   const int64_t slot = page * L.P + row % L.P;
-  const uint4* src = kv_new + t * kVec;
   uint4* dst = arena + ((own - shard_begin) * pool_pages * L.P + slot) * kVec;
-  uint4 v0 = __ldg(src + lane), v1 = __ldg(src + 32 + lane), v2;
-  if (lane < kVec - 64) v2 = __ldg(src + 64 + lane);
   dst[lane] = v0;
   dst[32 + lane] = v1;
   if (lane < kVec - 64) dst[64 + lane] = v2;
